@@ -1,0 +1,77 @@
+"""GPU parity of the decode-step weight stream (moe_decode_stack): L MoE layers on a bf16
+pre-norm residual stream, then the FP8 head with argmax / top-29.
+
+Teacher-forced per layer: the oracle's layer l is fed the device's r_l and must give the
+device's r_{l+1} to within one bf16 step (both round r_l + y once to bf16; the device's y is
+fp32, the oracle's float64, so a value on a rounding boundary may land on either side).
+The head is checked on the oracle's logits of bf16(RMSNorm(r_L)); argmax / top-k are
+compared where the oracle's margins exceed 1e-3.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from moe_decode_weight_gb300 import api, synth
+from oracle import lm_head as OL
+from oracle import stack as OS
+
+from _cases import Layer, bf16_to_np
+
+pytestmark = pytest.mark.gpu
+H = 2560
+
+
+def _bf16_step(v):
+    _, e = np.frexp(np.abs(v))
+    return np.ldexp(1.0, e - 1 - 7)
+
+
+@pytest.fixture(scope="module")
+def model():
+    layers = [Layer(seed=3, layer=l, num_experts=64, top_k=8, shared=True) for l in range(3)]
+    V = 20011
+    w = synth.lm_head_weight(1, V)
+    wd = w.cuda()
+    q = torch.empty((V, H), dtype=torch.uint8, device="cuda")
+    s = torch.empty(V, dtype=torch.float32, device="cuda")
+    head = api.quantize_lm_head_fp8(wd, q, s)
+    qo, so = OL.quantize_lm_head(bf16_to_np(w))
+    return layers, head, (qo, so), V
+
+
+@pytest.mark.parametrize("m", [1, 4])
+def test_stack_teacher_forced(model, m):
+    layers, head, (qo, so), V = model
+    L, k = len(layers), 29
+    r0 = synth.hidden_states(3, m, 0)
+    ws = torch.zeros(api.mdw_stack_workspace_bytes([l.weights for l in layers], head, m, k),
+                     dtype=torch.uint8, device="cuda")
+    resid = torch.zeros((L + 1, m, H), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((m,), -1, dtype=torch.int32, device="cuda")
+    ti = torch.full((m, k), -1, dtype=torch.int32, device="cuda")
+    lg = torch.zeros((m, V), dtype=torch.float32, device="cuda")
+    api.moe_decode_stack([l.weights for l in layers], head, r0.cuda(), am, ws, resid_out=resid,
+                         logits=lg, topk=k, topk_idx=ti)
+    assert api.mdw_device_status(ws) == 0
+    rs = resid.float().cpu().numpy()
+    assert np.array_equal(rs[0], bf16_to_np(r0))
+    for l, layer in enumerate(layers):
+        r_next, _, _ = OS.layer_step(rs[l], layer.oracle_dict(), layer.K)
+        diff = np.abs(rs[l + 1] - r_next)
+        assert np.all(diff <= _bf16_step(r_next) * 1.0001 + 1e-30), f"layer {l}"
+        assert (diff > 0).mean() < 0.01, f"layer {l}: {(diff > 0).mean():.4f} of r differ by one step"
+    xf = OS.rmsnorm_bf16(rs[L])
+    lo = OL.lm_head_fp8_logits(qo, so, xf)
+    lgn = lg.cpu().numpy()
+    assert np.max(np.abs(lgn - lo)) < 1e-2
+    order = np.stack([np.lexsort((np.arange(V), -lo[t])) for t in range(m)])
+    tin = ti.cpu().numpy()
+    for t in range(m):
+        vals = lo[t, order[t, :k + 1]]
+        clean = -np.diff(vals) > 1e-3
+        # compare the prefix of the ranking whose margins are all clean
+        n = k if clean.all() else int(np.argmin(clean))
+        assert np.array_equal(tin[t, :n], order[t, :n]), f"token {t}"
+        if clean[0]:
+            assert am.cpu().numpy()[t] == order[t, 0]
