@@ -1,0 +1,413 @@
+#!/usr/bin/env python3
+"""Benchmark of the full decode-step weight stream on GB300 (one JSON line on stdout).
+
+Workload (the pages' model, synthetic seeded weights): 42 MoE layers -- 512 routed experts,
+top-8, one shared expert, hidden 2,560, moe_intermediate 768, W4A8 MXFP4 -- on a bf16
+pre-norm residual stream, then the online-FP8 LM head (157,184 x 2,560) with argmax and
+top-29; M = 1 token per step (the batch-1 decode), and M = 4 (the verify window) reported
+alongside. ~68 GB of expert weights are resident; a step streams ~1.7 GB (M = 1), far more
+than the 129 MB L2, so no flush is needed between steps.
+
+A step is two C-ABI calls: moe_decode_stack (the 42 layers, one persistent kernel) and
+lm_head_fp8_rmsnorm (the final norm + head + argmax/top-29, one kernel). CUDA events on the
+launching stream time every step and each of the two kernels; `value` is microseconds per
+token over the timed region; `e2e` repeats the step with the input copied from pinned host
+memory and the argmax/top-29 copied back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the path has no exchange
+step); the reported time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/token & achieved HBM GB/s (vs 8 TB/s) for MoE+FP8 LM-head decode, M=1/4"
+NOMINAL_HBM_GBS = 8000.0
+L_DEFAULT, E, K_ROUTE, V, TOPK_VOCAB = 42, 512, 8, 157184, 29
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms while running (SM clock, throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines: list[str] = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- model
+
+
+def build_model(device, L: int, seed: int = 3):
+    from moe_decode_weight_gb300 import api, synth
+    layers = []
+    for l in range(L):
+        (w13q, w13s, w2q, w2s), sh = synth.layer_experts(seed, l, E, device=device)
+        wr = synth.router_weight(seed, l, E).to(device)
+        layers.append(api.MoeWeights(wr, w13q, w13s, w2q, w2s, tuple(sh), K_ROUTE))
+    w = synth.lm_head_weight(1, V).to(device)
+    q = torch.empty((V, 2560), dtype=torch.uint8, device=device)
+    s = torch.empty(V, dtype=torch.float32, device=device)
+    head = api.quantize_lm_head_fp8(w, q, s)
+    torch.cuda.synchronize()
+    return layers, head, w
+
+
+class Stepper:
+    """Buffers and the two C-ABI calls of one decode step for M tokens."""
+
+    def __init__(self, layers, head, m: int, device, pool: int = 8):
+        from moe_decode_weight_gb300 import api, synth
+        self.api, self.m, self.L = api, m, len(layers)
+        self.layers = layers
+        self.arr = api._layer_array(layers)
+        self.head = head
+        self.inputs = [synth.hidden_states(3, m, 100 + i).to(device) for i in range(pool)]
+        self.ws = torch.zeros(api.mdw_stack_workspace_bytes(layers, None, m, 1), dtype=torch.uint8,
+                              device=device)
+        self.hws = torch.zeros(api.mdw_lm_head_workspace_bytes(head, m, TOPK_VOCAB), dtype=torch.uint8,
+                               device=device)
+        self.resid = torch.zeros((self.L + 1, m, 2560), dtype=torch.bfloat16, device=device)
+        self.argmax = torch.zeros(m, dtype=torch.int32, device=device)
+        self.topk = torch.zeros((m, TOPK_VOCAB), dtype=torch.int32, device=device)
+
+    def layers_call(self, r0):
+        self.api.moe_decode_stack(self.arr, None, r0, None, self.ws, resid_out=self.resid)
+
+    def head_call(self):
+        self.api.lm_head_fp8_rmsnorm(self.head, self.resid[self.L], self.argmax, self.hws,
+                                     topk=TOPK_VOCAB, topk_idx=self.topk)
+
+    def unions(self, i: int):
+        """Realised routed union size of every layer for input i (untimed)."""
+        self.layers_call(self.inputs[i])
+        torch.cuda.synchronize()
+        hdr = self.ws[:1024].cpu().numpy().view(np.uint32)
+        st = int(hdr[0])
+        if st != 0:
+            raise RuntimeError(f"device status {self.api.STATUS.get(st, st)}")
+        return [int(u) for u in hdr[64:64 + self.L]]
+
+
+def time_steps(st: Stepper, steps: int, warmup: int, dist_barrier):
+    from moe_decode_weight_gb300 import roofline as R
+    P = len(st.inputs)
+    unions = [st.unions(i) for i in range(P)]
+    bytes_layers = [sum(R.moe_layer_bytes(u, st.m) for u in us) for us in unions]
+    bytes_head = R.head_fp8_bytes(0) + st.m * 2560 * 2 + st.m * (4 + 4 * TOPK_VOCAB)
+    for i in range(warmup):
+        st.layers_call(st.inputs[i % P])
+        st.head_call()
+    torch.cuda.synchronize()
+    dist_barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record()
+        st.layers_call(st.inputs[i % P])
+        ev[i][1].record()
+        st.head_call()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    dist_barrier()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    lay_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+    head_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    b_lay = [bytes_layers[i % P] for i in range(steps)]
+    return dict(total_ms=total_ms, layer_ms=lay_ms, head_ms=head_ms, bytes_layers=b_lay,
+                bytes_head=bytes_head, unions=unions)
+
+
+def time_e2e(st: Stepper, steps: int, warmup: int):
+    """The same step through the public API with the input in pinned host memory and the
+    argmax / top-29 read back into pinned host memory inside the timed region."""
+    P = len(st.inputs)
+    host_in = [x.cpu().pin_memory() for x in st.inputs]
+    dev_in = torch.empty_like(st.inputs[0])
+    out_am = torch.empty(st.m, dtype=torch.int32).pin_memory()
+    out_tk = torch.empty((st.m, TOPK_VOCAB), dtype=torch.int32).pin_memory()
+
+    def one(i):
+        dev_in.copy_(host_in[i % P], non_blocking=True)
+        st.layers_call(dev_in)
+        st.head_call()
+        out_am.copy_(st.argmax, non_blocking=True)
+        out_tk.copy_(st.topk, non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d = st.m * 2560 * 2
+    d2h = st.m * 4 + st.m * TOPK_VOCAB * 4
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+# ----------------------------------------------------------------------------- oracle
+
+
+def oracle_sample(m: int = 1, n_layers: int = 8, frac: int = 8):
+    """Time the float64 oracle on a bounded sample of the M-token step: n_layers of the 42
+    layers and a fraction of the head's rows; extrapolated to one full step."""
+    from moe_decode_weight_gb300 import synth
+    from oracle import lm_head as OL
+    from oracle import stack as OS
+
+    seed = 3
+    r = synth.hidden_states(3, m, 100).float().numpy()
+    layers, cache = [], {}
+    for l in range(n_layers):
+        wr = synth.router_weight(seed, l, E).float().numpy()
+
+        def ex(e, l=l):
+            key = (l, e)
+            if key not in cache:
+                cache[key] = tuple(t.numpy() for t in synth.expert_tensors(seed, l, e))
+            return cache[key]
+        layers.append(dict(wr=wr, experts=ex, shared=ex(synth.SHARED_EXPERT)))
+    # warm the expert cache (input generation is not oracle work)
+    rr = r
+    for layer in layers:
+        rr, _, _ = OS.layer_step(rr, layer, K_ROUTE)
+    rows = V // frac
+    w = synth.lm_head_weight(1, rows).float().numpy()    # the first rows of the same stream
+    t0 = time.perf_counter()
+    rr = r
+    for layer in layers:
+        rr, _, _ = OS.layer_step(rr, layer, K_ROUTE)
+    t1 = time.perf_counter()
+    q, s = OL.quantize_lm_head(w)           # untimed: the head is quantised once at init
+    t2 = time.perf_counter()
+    OL.lm_head_fp8_logits(q, s, OS.rmsnorm_bf16(rr))
+    t3 = time.perf_counter()
+    per_step_s = (t1 - t0) * (L_DEFAULT / n_layers) + (t3 - t2) * frac
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dict(us_per_token=per_step_s * 1e6 / m, cores=cores,
+                sample=f"{n_layers} of {L_DEFAULT} layers (M={m}) + 1/{frac} of the 157,184 head rows, "
+                       f"float64 numpy oracle, extrapolated to one full step",
+                cpu_seconds=(t1 - t0) + (t3 - t2))
+
+
+# ----------------------------------------------------------------------------- arms
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    res = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(m=args.m, n_layers=2, frac=32)
+        if i >= args.warmup:
+            res.append(r)
+    us = float(np.median([r["us_per_token"] for r in res]))
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/token",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us * args.m / 1000.0, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _workload(args.m), "M": args.m},
+            "cpu_baseline": {"value": us, "unit": "us/token", "cores": res[0]["cores"], "kind": "oracle",
+                             "sample": res[0]["sample"]},
+            "e2e": {"value": us, "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _workload(m: int) -> str:
+    return (f"decode step: 42 MoE layers (512 experts top-8 + 1 shared, H 2560, I 768, W4A8 MXFP4, "
+            f"bf16 pre-norm residual) + online-FP8 LM head 157184x2560 + argmax/top-29, M={m}")
+
+
+def run_gpu(args, rank: int, world: int):
+    from moe_decode_weight_gb300 import api
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    api.lib()
+    dist_barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    peak, peak_kind = _peaks()
+
+    layers, head, _w_bf16 = build_model(device, args.layers)
+    st = Stepper(layers, head, args.m, device)
+    clocks = ClockSampler(local).start()
+    res = time_steps(st, args.steps, args.warmup, dist_barrier)
+    clk = clocks.stop()
+    total_ms = res["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    us_token = ms_step * 1000.0 / (args.m * world)
+    lay_ms = float(np.mean(res["layer_ms"]))
+    head_ms = float(np.mean(res["head_ms"]))
+    b_lay = float(np.mean(res["bytes_layers"]))
+    b_step = b_lay + res["bytes_head"]
+    lay_gbs = b_lay / (lay_ms * 1e6)
+    head_gbs = res["bytes_head"] / (head_ms * 1e6)
+    step_gbs = b_step / (ms_step * 1e6)
+
+    e2e_ms, h2d, d2h = time_e2e(st, args.steps, args.warmup)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    extra = {}
+    if not args.no_m4 and args.m == 1:
+        st4 = Stepper(layers, head, 4, device)
+        r4 = time_steps(st4, args.steps, args.warmup, dist_barrier)
+        ms4 = r4["total_ms"] / args.steps
+        b4 = float(np.mean(r4["bytes_layers"])) + r4["bytes_head"]
+        lay4 = float(np.mean(r4["layer_ms"]))
+        extra["m4"] = {"us_per_step": ms4 * 1000, "us_per_token": ms4 * 250.0,
+                       "achieved_gbs": b4 / (ms4 * 1e6), "frac_of_8tbs": b4 / (ms4 * 1e6) / NOMINAL_HBM_GBS,
+                       "layer_stack_us": lay4 * 1000,
+                       "layer_stack_gbs": float(np.mean(r4["bytes_layers"])) / (lay4 * 1e6),
+                       "head_us": float(np.mean(r4["head_ms"])) * 1000,
+                       "mean_union": float(np.mean([np.mean(u) for u in r4["unions"]])),
+                       "verify_cost_ratio": ms4 / ms_step}
+        del st4
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        try:
+            o = oracle_sample(m=args.m)
+            cpu = {"value": o["us_per_token"], "unit": "us/token", "cores": o["cores"], "kind": "oracle",
+                   "sample": o["sample"]}
+        except Exception as e:        # the baseline is reported, not required
+            cpu = {"value": None, "unit": "us/token", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
+    line = {
+        "metric": METRIC, "value": us_token, "unit": "us/token", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": _workload(args.m), "M": args.m, "layers": args.layers, "experts": E,
+                   "top_k": K_ROUTE, "hidden": 2560, "inter": 768, "vocab": V,
+                   "l2": "inputs larger than L2: each step streams %.2f GB of weights" % (b_step / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+        "frac_of_measured": step_gbs / peak,
+        "layer_stack_us": lay_ms * 1000, "layer_us": lay_ms * 1000 / args.layers,
+        "layer_stack_gbs": lay_gbs, "head_us": head_ms * 1000, "head_gbs": head_gbs,
+        "bytes_per_step": b_step,
+        "roofline": {"bound": "hbm", "achieved": lay_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": lay_gbs / peak, "traffic": None,
+                     "kernel": "moe_persistent_kernel (42 layers, one launch)",
+                     "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_ms * 1000.0 / (args.steps * args.m * world), "unit": "us/token",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=L_DEFAULT)
+    ap.add_argument("--no-m4", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        backend = "nccl" if args.impl == "gb300" else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank)
+        else:
+            run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -129,7 +129,8 @@ typedef struct mdw_lm_head {
  * the union of the routed selections in ascending expert id); pairs are ordered by slot,
  * then by token. In moe_decode_stack the buffers hold the last layer's values. */
 typedef struct mdw_moe_ws_layout {
-  size_t header;     /* uint32 [64]: [0] device status, [2] S, [3] P, [4] routed slots */
+  size_t header;     /* uint32 [256]: [0] device status, [2] S, [3] P, [4] routed slots;
+                        [64 + l] routed union size of layer l (moe_decode_stack) */
   size_t xq;         /* uint8 [M][H] E4M3 codes of the quantised expert input */
   size_t sx;         /* fp32 [M] its per-token scales */
   size_t logits;     /* fp32 [M][E] router logits */
@@ -230,13 +231,24 @@ size_t mdw_stack_workspace_bytes(const mdw_moe_weights* layers, int32_t L, const
  *   x_l = bf16(RMSNorm(r_l));  r_{l+1} = bf16(r_l + MoE_l(x_l));
  *   logits = head(bf16(RMSNorm(r_L))), then argmax / top-k.
  * layers : HOST array of L (1..128) layer descriptors (read during the call only).
+ * head   : the FP8 head (fmt MDW_FMT_FP8_E4M3_ROWSCALE), or NULL to run the L layers only
+ *          (then resid_out is required, r_L is resid_out[L], and the head outputs are
+ *          ignored; lm_head_fp8_rmsnorm finishes the step).
  * r0_bf16: device bf16 [M][H] initial residual.
  * resid_out : NULL or device bf16 [L+1][M][H]: every r_l, for inspection.
- * Other outputs as lm_head_fp8. head->fmt must be MDW_FMT_FP8_E4M3_ROWSCALE. */
+ * Other outputs as lm_head_fp8. The workspace header's word 64 + l holds the number of
+ * distinct routed experts of layer l (the window's union). */
 mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_lm_head* head,
                             int32_t M, const void* r0_bf16, void* resid_out, float* logits,
                             int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val,
                             void* ws, size_t ws_bytes, mdw_stream_t stream);
+
+/* The last step of moe_decode_stack on its own: lm_head_fp8 applied to bf16(RMSNorm(r)),
+ * RMSNorm with unit gain and eps 1e-6 in fp32, r_bf16 = device bf16 [M][H] (the residual
+ * stream after the last layer). Arguments otherwise as lm_head_fp8. */
+mdw_status lm_head_fp8_rmsnorm(const mdw_lm_head* head, int32_t M, const void* r_bf16, float* logits,
+                               int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val,
+                               void* ws, size_t ws_bytes, mdw_stream_t stream);
 
 /* Synchronises `stream`, then returns the device status word that the last call using
  * this workspace left (MDW_OK, MDW_ERR_TIMEOUT or MDW_ERR_DEVICE_BOUNDS), or MDW_ERR_CUDA

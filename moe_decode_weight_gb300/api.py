@@ -28,7 +28,8 @@ MAX_M, MAX_TOPK, MAX_VOCAB_TOPK, MAX_EXPERTS = 16, 8, 32, 512
 # exported symbols declared in include/moe_decode_weight.h
 SYMBOLS = ["mdw_status_string", "mdw_version", "mdw_moe_workspace_bytes", "mdw_moe_workspace_layout",
            "moe_decode_layer", "quantize_lm_head_fp8", "mdw_lm_head_bf16_init",
-           "mdw_lm_head_workspace_bytes", "lm_head_fp8", "lm_head_bf16", "mdw_stack_workspace_bytes",
+           "mdw_lm_head_workspace_bytes", "lm_head_fp8", "lm_head_bf16", "lm_head_fp8_rmsnorm",
+           "mdw_stack_workspace_bytes",
            "moe_decode_stack", "mdw_device_status"]
 
 
@@ -85,7 +86,7 @@ def lib() -> C.CDLL:
     L.mdw_lm_head_bf16_init.argtypes = [vp, i64, i32, C.POINTER(LMHeadC)]
     L.mdw_lm_head_workspace_bytes.restype = sz
     L.mdw_lm_head_workspace_bytes.argtypes = [C.POINTER(LMHeadC), i32, i32]
-    for name in ("lm_head_fp8", "lm_head_bf16"):
+    for name in ("lm_head_fp8", "lm_head_bf16", "lm_head_fp8_rmsnorm"):
         f = getattr(L, name)
         f.restype = C.c_int
         f.argtypes = [C.POINTER(LMHeadC), i32, vp, vp, vp, i32, vp, vp, vp, sz, vp]
@@ -210,22 +211,33 @@ def lm_head_bf16(head: LMHead, h: torch.Tensor, argmax_out: torch.Tensor, ws: to
     _head("lm_head_bf16", head, h, argmax_out, ws, logits, topk, topk_idx, topk_val, stream)
 
 
+def lm_head_fp8_rmsnorm(head: LMHead, r: torch.Tensor, argmax_out: torch.Tensor, ws: torch.Tensor,
+                        logits=None, topk: int = 1, topk_idx=None, topk_val=None, stream=None) -> None:
+    _head("lm_head_fp8_rmsnorm", head, r, argmax_out, ws, logits, topk, topk_idx, topk_val, stream)
+
+
 def _layer_array(layers):
+    """ctypes array of layer descriptors (a prebuilt array is passed through unchanged)."""
+    if isinstance(layers, C.Array):
+        return layers
     arr = (MoeWeightsC * len(layers))()
     for i, w in enumerate(layers):
         arr[i] = w.c
     return arr
 
 
-def mdw_stack_workspace_bytes(layers, head: LMHead, m: int, topk: int) -> int:
-    return lib().mdw_stack_workspace_bytes(_layer_array(layers), len(layers), C.byref(head.c), m, topk)
+def mdw_stack_workspace_bytes(layers, head, m: int, topk: int) -> int:
+    hc = C.byref(head.c) if head is not None else None
+    return lib().mdw_stack_workspace_bytes(_layer_array(layers), len(layers), hc, m, topk)
 
 
-def moe_decode_stack(layers, head: LMHead, r0: torch.Tensor, argmax_out: torch.Tensor, ws: torch.Tensor,
+def moe_decode_stack(layers, head, r0: torch.Tensor, argmax_out, ws: torch.Tensor,
                      resid_out=None, logits=None, topk: int = 1, topk_idx=None, topk_val=None,
                      stream=None) -> None:
+    """head=None runs the layers only (resid_out required); lm_head_fp8_rmsnorm finishes."""
     arr = _layer_array(layers)
-    code = lib().moe_decode_stack(arr, len(layers), C.byref(head.c), r0.shape[0], _ptr(r0), _ptr(resid_out),
+    hc = C.byref(head.c) if head is not None else None
+    code = lib().moe_decode_stack(arr, len(layers), hc, r0.shape[0], _ptr(r0), _ptr(resid_out),
                                   _ptr(logits), _ptr(argmax_out), topk, _ptr(topk_idx), _ptr(topk_val),
                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check("moe_decode_stack", code)

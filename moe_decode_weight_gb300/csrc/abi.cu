@@ -137,7 +137,7 @@ mdw_status head_call(const mdw_lm_head* head, int fmt, int32_t M, const void* h_
 
 mdw_status head_entry(int fmt, const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
                       int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val, void* ws,
-                      size_t ws_bytes, cudaStream_t s) {
+                      size_t ws_bytes, cudaStream_t s, int norm_input = 0) {
   mdw_status st = check_head(head, fmt);
   if (st != MDW_OK) return st;
   if (M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK || head->vocab < topk)
@@ -147,8 +147,8 @@ mdw_status head_entry(int fmt, const mdw_lm_head* head, int32_t M, const void* h
   if (head_grid() <= 0) return MDW_ERR_CUDA;
   uint8_t* base = static_cast<uint8_t*>(ws);
   if (cudaMemsetAsync(base, 0, kHdrWords * 4, s) != cudaSuccess) return MDW_ERR_CUDA;
-  return head_call(head, fmt, M, h_bf16, 0, logits, argmax_out, topk, topk_idx, topk_val,
-                   reinterpret_cast<uint32_t*>(base), base + 256, s);
+  return head_call(head, fmt, M, h_bf16, norm_input, logits, argmax_out, topk, topk_idx, topk_val,
+                   reinterpret_cast<uint32_t*>(base), base + kHdrWords * 4, s);
 }
 
 }  // namespace
@@ -256,7 +256,7 @@ size_t mdw_lm_head_workspace_bytes(const mdw_lm_head* head, int32_t M, int32_t t
   if (!head || M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK) return 0;
   const int g = head_grid();
   if (g <= 0) return 0;
-  return 256 + align_up((size_t)g * M * topk * 4, 256) + align_up((size_t)g * M * topk * 4, 256);
+  return kHdrWords * 4 + align_up((size_t)g * M * topk * 4, 256) + align_up((size_t)g * M * topk * 4, 256);
 }
 
 mdw_status lm_head_fp8(const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
@@ -273,9 +273,17 @@ mdw_status lm_head_bf16(const mdw_lm_head* head, int32_t M, const void* h_bf16, 
                     ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+mdw_status lm_head_fp8_rmsnorm(const mdw_lm_head* head, int32_t M, const void* r_bf16, float* logits,
+                               int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val, void* ws,
+                               size_t ws_bytes, mdw_stream_t stream) {
+  return head_entry(MDW_FMT_FP8_E4M3_ROWSCALE, head, M, r_bf16, logits, argmax_out, topk, topk_idx, topk_val,
+                    ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), 1);
+}
+
 size_t mdw_stack_workspace_bytes(const mdw_moe_weights* layers, int32_t L, const mdw_lm_head* head,
                                  int32_t M, int32_t topk) {
-  if (!layers || L < 1 || L > kMaxLayers || M < 1 || M > MDW_MAX_M || !head) return 0;
+  if (!layers || L < 1 || L > kMaxLayers || M < 1 || M > MDW_MAX_M) return 0;
+  if (!head) topk = 1;
   if (topk < 1 || topk > MDW_MAX_VOCAB_TOPK) return 0;
   int E = 0, K = 0;
   for (int l = 0; l < L; ++l) {
@@ -291,8 +299,13 @@ mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_
                             int32_t topk, int32_t* topk_idx, float* topk_val, void* ws, size_t ws_bytes,
                             mdw_stream_t stream) {
   if (!layers || L < 1 || L > kMaxLayers) return MDW_ERR_INVALID_ARG;
-  mdw_status st = check_head(head, MDW_FMT_FP8_E4M3_ROWSCALE);
-  if (st != MDW_OK) return st;
+  mdw_status st = MDW_OK;
+  if (head) {
+    st = check_head(head, MDW_FMT_FP8_E4M3_ROWSCALE);
+    if (st != MDW_OK) return st;
+  } else if (!resid_out) {
+    return MDW_ERR_INVALID_ARG;
+  }
   int E = 0, K = 0;
   for (int l = 0; l < L; ++l) {
     st = check_weights(&layers[l]);
@@ -303,10 +316,12 @@ mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_
     E = layers[l].num_experts;
     K = layers[l].top_k;
   }
-  if (M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK || head->vocab < topk)
+  if (M < 1 || M > MDW_MAX_M) return MDW_ERR_INVALID_ARG;
+  if (head && (topk < 1 || topk > MDW_MAX_VOCAB_TOPK || head->vocab < topk || !argmax_out ||
+               !al16_or_null(logits)))
     return MDW_ERR_INVALID_ARG;
-  if (!al16(r0_bf16) || !al16_or_null(resid_out) || !al16_or_null(logits) || !argmax_out || !al16(ws))
-    return MDW_ERR_INVALID_ARG;
+  if (!head) topk = 1;
+  if (!al16(r0_bf16) || !al16_or_null(resid_out) || !al16(ws)) return MDW_ERR_INVALID_ARG;
   const MoeWs lay = moe_ws_layout(M, E, K, true, topk);
   if (ws_bytes < lay.total) return MDW_ERR_WORKSPACE_TOO_SMALL;
   if (moe_grid() * 32 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
@@ -334,7 +349,7 @@ mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_
   if (st == MDW_OK) st = cuda_status(launch_moe(*p, s));
   const __nv_bfloat16* rL = p->resid + (size_t)(p->resid_pingpong ? (L & 1) : L) * M * kH;
   delete p;
-  if (st != MDW_OK) return st;
+  if (st != MDW_OK || !head) return st;
   return head_call(head, MDW_FMT_FP8_E4M3_ROWSCALE, M, rL, 1, logits, argmax_out, topk, topk_idx, topk_val,
                    reinterpret_cast<uint32_t*>(base + lay.lay.header), base + lay.cand, s);
 }

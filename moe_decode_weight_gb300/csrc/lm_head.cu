@@ -352,7 +352,7 @@ cudaError_t launch_head_any(const HeadParams& p, cudaStream_t s) {
 }  // namespace
 
 size_t head_ws_bytes(int M, int topk, int grid) {
-  return (size_t)grid * M * topk * 8 + 256;
+  return (size_t)grid * M * topk * 8 + 512;
 }
 
 cudaError_t launch_head_fp8(const HeadParams& p, cudaStream_t s) { return launch_head_any<true>(p, s); }

@@ -32,7 +32,8 @@ enum HeaderWord : int {
   kHdrPairs = 3,      // P: (token, expert) pairs of the last layer
   kHdrRouted = 4,     // routed slots of the last layer
   kHdrDoneCtr = 5,    // last-block-done counter of the LM head
-  kHdrWords = 64
+  kHdrUnions = 64,    // [64 + l]: routed union size of layer l (stack)
+  kHdrWords = 256
 };
 
 // ------------------------------------------------------------------ status

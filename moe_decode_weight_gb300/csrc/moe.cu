@@ -194,7 +194,7 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
 
 // ------------------------------------------------------------------ P2: top-k + dedup
 
-__device__ void route_tokens(const MoeParams& p, Tables& tb) {
+__device__ void route_tokens(const MoeParams& p, Tables& tb, int layer) {
   const int M = p.M, E = p.E, K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < MDW_MAX_EXPERTS / 32) tb.bitmap[threadIdx.x] = 0;
@@ -347,6 +347,7 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb) {
       p.hdr[kHdrSlots] = tb.n_slots;
       p.hdr[kHdrPairs] = tb.n_pairs;
       p.hdr[kHdrRouted] = tb.n_routed;
+      if (layer < kHdrWords - kHdrUnions) p.hdr[kHdrUnions + layer] = tb.n_routed;
     }
   }
 }
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
       gate_up_range<MAXM>(p, L, smem, tb, j0, j1, 0);
     }
     if (!bar.wait()) return;
-    route_tokens(p, tb);
+    route_tokens(p, tb, layer);
     __syncthreads();
     if (tb.bad) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
     {

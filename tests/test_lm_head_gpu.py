@@ -46,13 +46,20 @@ def test_quantize_bit_exact(V):
 
 
 def _hidden(q, s, m, k, seed=1, bf16_w=None):
-    for attempt in range(100):
-        h = synth.hidden_states(seed, m, attempt)
-        hx = bf16_to_np(h)
-        lg = OL.lm_head_fp8_logits(q, s, hx) if bf16_w is None else OL.lm_head_bf16_logits(bf16_w, hx)
-        if topk_gap_ok(lg, k):
-            return h, lg
-    raise RuntimeError("no hidden state with clean top-k gaps")
+    """Per token, redraw (seeded attempts) until the oracle's top-(k+1) logits are 1e-3 apart."""
+    rows, logits = [], []
+    for t in range(m):
+        for attempt in range(100):
+            h = synth.hidden_states(1000 * seed + t, 1, attempt)
+            hx = bf16_to_np(h)
+            lg = OL.lm_head_fp8_logits(q, s, hx) if bf16_w is None else OL.lm_head_bf16_logits(bf16_w, hx)
+            if topk_gap_ok(lg, k):
+                rows.append(h)
+                logits.append(lg)
+                break
+        else:
+            raise RuntimeError("no hidden state with clean top-k gaps")
+    return torch.cat(rows, 0), np.concatenate(logits, 0)
 
 
 def _run_head(fn, head, h, V, k, with_logits=True):
