@@ -190,6 +190,37 @@ mdw_status moe_decode_layer(const mdw_moe_weights* w, int32_t M, const void* x_b
                             const int32_t* topk_override, int32_t* topk_ids_out,
                             float* topk_w_out, void* ws, size_t ws_bytes, mdw_stream_t stream);
 
+/* Bytes of the scratch array that the library holds on every GPU it runs on, for
+ * moe_decode_layer_noalloc (1 MiB). */
+#define MDW_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* moe_decode_layer without a caller workspace. The pages have no counterpart: this is an
+ * integration entry point of this library.
+ *
+ * For callers that cannot allocate device memory: code running inside a host framework
+ * that owns the whole device-memory budget and forbids further allocations, plain C callers
+ * without an allocator, and latency-critical loops where cudaMalloc / cudaFree would
+ * implicitly synchronise the device. The caller passes inputs and outputs exactly as for
+ * moe_decode_layer (same meaning, layout and validation); the scratch is a fixed array of
+ * MDW_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that loads the
+ * library holds until the process exits. Calls that moe_decode_layer accepts all fit; a
+ * shape whose workspace would exceed the array returns MDW_ERR_WORKSPACE_TOO_SMALL.
+ *
+ * Nothing is allocated: no cudaMalloc / cudaFree, no allocating library routine, no host
+ * heap. The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture. Every call on a device shares the one array and re-zeroes the part that must
+ * start at zero; the array keeps the last call's intermediates otherwise. Calls whose work
+ * overlaps on the GPU (different streams without ordering) race on the array.
+ *
+ * device_status_out: NULL or a device uint32 that receives the call's device status word
+ * (MDW_OK, MDW_ERR_TIMEOUT or MDW_ERR_DEVICE_BOUNDS) in stream order. */
+mdw_status moe_decode_layer_noalloc(const mdw_moe_weights* w, int32_t M, const void* x_bf16, void* y,
+                                    int32_t y_is_fp32, const void* residual,
+                                    const int32_t* topk_override, int32_t* topk_ids_out,
+                                    float* topk_w_out, uint32_t* device_status_out,
+                                    mdw_stream_t stream);
+
 /* Online FP8 quantisation of a BF16 LM head ("Online FP8 quantization halves the LM head
  * weight reads": done once, when the head is constructed). Per vocabulary row v:
  * scale_v = amax_v / 448 in fp32 (1 for an all-zero row); q[v][h] = E4M3(w[v][h] / scale_v),

@@ -30,7 +30,7 @@ SYMBOLS = ["mdw_status_string", "mdw_version", "mdw_moe_workspace_bytes", "mdw_m
            "moe_decode_layer", "quantize_lm_head_fp8", "mdw_lm_head_bf16_init",
            "mdw_lm_head_workspace_bytes", "lm_head_fp8", "lm_head_bf16", "lm_head_fp8_rmsnorm",
            "mdw_stack_workspace_bytes",
-           "moe_decode_stack", "mdw_device_status"]
+           "moe_decode_stack", "mdw_device_status", "moe_decode_layer_noalloc"]
 
 
 class MdwError(RuntimeError):
@@ -97,6 +97,8 @@ def lib() -> C.CDLL:
                                    i32, vp, vp, vp, sz, vp]
     L.mdw_device_status.restype = C.c_int
     L.mdw_device_status.argtypes = [vp, vp]
+    L.moe_decode_layer_noalloc.restype = C.c_int
+    L.moe_decode_layer_noalloc.argtypes = [C.POINTER(MoeWeightsC), i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
     _lib = L
     return L
 
@@ -171,6 +173,18 @@ def moe_decode_layer(w: MoeWeights, x: torch.Tensor, y: torch.Tensor, ws: torch.
                                   _ptr(topk_w_out), _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream))
     _check("moe_decode_layer", code)
+
+
+def moe_decode_layer_noalloc(w: MoeWeights, x: torch.Tensor, y: torch.Tensor, residual=None,
+                             topk_override=None, topk_ids_out=None, topk_w_out=None,
+                             device_status_out=None, stream=None) -> None:
+    """moe_decode_layer for callers that cannot allocate device memory: the library's own
+    fixed scratch array replaces the workspace (see the C declaration for its limits)."""
+    code = lib().moe_decode_layer_noalloc(C.byref(w.c), x.shape[0], _ptr(x), _ptr(y),
+                                          int(y.dtype == torch.float32), _ptr(residual),
+                                          _ptr(topk_override), _ptr(topk_ids_out), _ptr(topk_w_out),
+                                          _ptr(device_status_out), _stream(stream))
+    _check("moe_decode_layer_noalloc", code)
 
 
 def quantize_lm_head_fp8(w_bf16: torch.Tensor, q_out: torch.Tensor, scale_out: torch.Tensor,
