@@ -18,7 +18,7 @@ int device_sm_count() {
   return n;
 }
 int moe_grid() { return device_sm_count(); }
-int head_grid() { return device_sm_count(); }
+int head_grid() { const int n = device_sm_count(); return n > 256 ? 256 : n; }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

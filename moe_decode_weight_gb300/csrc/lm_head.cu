@@ -22,9 +22,14 @@ namespace {
 constexpr int kHeadThreads = kThreads;
 constexpr int kMaxTK = 32;               // candidates per token per warp (lane-distributed)
 constexpr int kMergeCap = 256;           // compacted candidates per warp during a merge
+constexpr int kMaxHeadGrid = 256;        // blocks of the head kernel (one per SM)
 
-__host__ __device__ inline size_t head_smem_bytes(int M) {
-  return (size_t)M * kH * 4 + (size_t)kWarps * (2 * kMaxTK + 2 * kMergeCap + 2 * kMaxTK) * 4;
+__host__ __device__ inline size_t head_smem_bytes(int M, int MAXM) {
+  // xs [M][H] fp32 (its bytes later hold the warp lists [MAXM][warps][32] x 2 and the global
+  // merge's [M][kMergeCap] x 2), thresholds / counters [MAXM] x 3, results [MAXM][32] x 2,
+  // per-warp merge scratch [warps][kMergeCap] x 2
+  return (size_t)M * kH * 4 + (size_t)MAXM * 12 + (size_t)MAXM * kMaxTK * 8 +
+         (size_t)kWarps * kMergeCap * 8 + 64;
 }
 
 // ------------------------------------------------------------------ quantisation
@@ -196,47 +201,93 @@ __device__ __forceinline__ void row_dot(const RowLoad<FP8>& ld, const float* xs,
     if (t < M) acc[t] = warp_sum(acc[t]);
 }
 
+// tk-th best (value, index) among the warp's register-held candidates (PER per lane),
+// by tk rounds of warp arg-max; every lane gets the result.
+template <int PER>
+__device__ void warp_kth(const float (&v)[PER], const int (&ix)[PER], int tk, float& kv, int& ki) {
+  float pv = INFINITY;
+  int pi = -1;
+  for (int r = 0; r < tk; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (beats(pv, pi, v[j], ix[j]) && beats(v[j], ix[j], bv, bi)) { bv = v[j]; bi = ix[j]; }
+    warp_argmax(bv, bi);
+    pv = bv; pi = bi;
+  }
+  kv = pv; ki = pi;
+}
+
 template <bool FP8, int MAXM>
 __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  float* xs = reinterpret_cast<float*>(smem);                             // [M][H] fp32
-  float* mv = reinterpret_cast<float*>(smem + (size_t)p.M * kH * 4);      // warp lists
-  int* mi = reinterpret_cast<int*>(mv + kWarps * kMaxTK);
-  float* tv_s = reinterpret_cast<float*>(mi + kWarps * kMaxTK);           // per-warp scratch
+  // xs [M][H] fp32 hidden states; after the row loop the same bytes hold the warps' lists
+  // (mv / mi) and, in the last block, the global merge's compacted candidates
+  float* xs = reinterpret_cast<float*>(smem);
+  float* mv = xs;                                                         // [M][warps][32]
+  int* mi = reinterpret_cast<int*>(mv + MAXM * kWarps * kMaxTK);
+  float* thv = reinterpret_cast<float*>(smem + (size_t)p.M * kH * 4);     // [M] per-token thresholds
+  int* thi = reinterpret_cast<int*>(thv + MAXM);
+  int* cnt = thi + MAXM;                                                  // [M] compaction counters
+  float* ov = reinterpret_cast<float*>(cnt + MAXM);                       // [M][32] results
+  int* oi = reinterpret_cast<int*>(ov + MAXM * kMaxTK);
+  float* tv_s = reinterpret_cast<float*>(oi + MAXM * kMaxTK);             // per-warp scratch (block merge)
   int* ti_s = reinterpret_cast<int*>(tv_s + kWarps * kMergeCap);
-  float* ov_s = reinterpret_cast<float*>(ti_s + kWarps * kMergeCap);      // per-warp results
-  int* oi_s = reinterpret_cast<int*>(ov_s + kWarps * kMaxTK);
-  __shared__ float th_v[kWarps];
-  __shared__ int th_i[kWarps];
   __shared__ int is_last;
   const int M = p.M, tk = p.topk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
   const long long v0 = blockIdx.x * p.V / G, v1 = (blockIdx.x + 1) * p.V / G;
   constexpr int ROWB = FP8 ? kH : 2 * kH;
+  constexpr int NC = FP8 ? 5 : 10;
+  constexpr int EPC = FP8 ? 16 : 8;
+  constexpr int kAhead = 4;                 // rows a warp prefetches into L2 ahead of use
 
-  // hidden states -> fp32 shared memory (optionally bf16(RMSNorm(.)) first)
-  for (int t = warp; t < M; t += kWarps) {
-    const __nv_bfloat16* src = p.x + (size_t)t * kH;
-    float ss = 0.f;
-    for (int e = lane; e < kH; e += 32) {
-      const float a = __bfloat162float(src[e]);
-      xs[(size_t)t * kH + e] = a;
-      ss = fmaf(a, a, ss);
+  // prefetch this warp's first rows while the hidden states are prepared
+  if (lane == 0)
+    for (int a = 0; a < kAhead; ++a) {
+      const long long v = v0 + warp + (long long)a * kWarps;
+      if (v < v1) prefetch_l2(p.w + v * ROWB, ROWB);
     }
+
+  // hidden states -> fp32 shared memory (optionally bf16(RMSNorm(.)) first); all threads,
+  // 16-byte loads, fixed-order per-token reductions
+  {
+    float* part = tv_s;                      // [M][10] partial sums of squares
+    for (int c = threadIdx.x; c < M * (kH / 8); c += blockDim.x) {
+      const int t = c / (kH / 8), i = c % (kH / 8);
+      const uint4 u = ld_cg16(reinterpret_cast<const uint4*>(p.x + (size_t)t * kH) + i);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a = __uint_as_float(w4[k] << 16), b = __uint_as_float(w4[k] & 0xFFFF0000u);
+        xs[(size_t)t * kH + 8 * i + 2 * k] = a;
+        xs[(size_t)t * kH + 8 * i + 2 * k + 1] = b;
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+      ss = warp_sum(ss);                    // a warp's 32 chunks belong to one token (320 % 32 == 0)
+      if (lane == 0) part[t * 10 + i / 32] = ss;
+    }
+    __syncthreads();
     if (p.norm_input) {
-      ss = warp_sum(ss);
-      const float inv = rsqrtf(ss / (float)kH + 1e-6f);
-      for (int e = lane; e < kH; e += 32)
-        xs[(size_t)t * kH + e] = __bfloat162float(__float2bfloat16_rn(xs[(size_t)t * kH + e] * inv));
+      if (threadIdx.x < M) {
+        float ss = 0.f;
+        for (int j = 0; j < 10; ++j) ss += part[threadIdx.x * 10 + j];
+        thv[threadIdx.x] = rsqrtf(ss / (float)kH + 1e-6f);
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < M * kH; e += blockDim.x)
+        xs[e] = __bfloat162float(__float2bfloat16_rn(xs[e] * thv[e / kH]));
+      __syncthreads();
     }
   }
-  __syncthreads();
   float xr[80];
-  constexpr int EPC = FP8 ? 16 : 8;
   if (MAXM == 1) {
 #pragma unroll
-    for (int c = 0; c < (FP8 ? 5 : 10); ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int k = 0; k < EPC; ++k) xr[c * EPC + k] = xs[(32 * c + lane) * EPC + k];
   }
@@ -248,51 +299,62 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   auto load_row = [&](long long v, RowLoad<FP8>& ld) {
     const uint4* src = reinterpret_cast<const uint4*>(p.w + v * ROWB);
 #pragma unroll
-    for (int c = 0; c < (FP8 ? 5 : 10); ++c) ld.q[c] = ldg_stream16(src + 32 * c + lane);
+    for (int c = 0; c < NC; ++c) ld.q[c] = ldg_stream16(src + 32 * c + lane);
   };
   long long v = v0 + warp;
   RowLoad<FP8> cur, nxt;
-  if (v < v1) load_row(v, cur);
+  float sc_cur = 1.f, sc_nxt = 1.f;
+  if (v < v1) { load_row(v, cur); if (FP8) sc_cur = p.row_scale[v]; }
   while (v < v1) {
     const long long vn = v + kWarps;
-    if (vn < v1) load_row(vn, nxt);
+    if (lane == 0) {
+      const long long vp = v + (long long)kAhead * kWarps;
+      if (vp < v1) prefetch_l2(p.w + vp * ROWB, ROWB);
+    }
+    if (vn < v1) { load_row(vn, nxt); if (FP8) sc_nxt = p.row_scale[vn]; }
     float acc[MAXM];
     row_dot<FP8, MAXM>(cur, xs, xr, M, lane, acc);
-    const float sc = FP8 ? p.row_scale[v] : 1.0f;
 #pragma unroll
     for (int t = 0; t < MAXM; ++t) {
       if (t < M) {
-        const float logit = acc[t] * sc;
+        const float logit = acc[t] * sc_cur;
         if (p.logits && lane == 0) p.logits[(size_t)t * p.V + v] = logit;
         list_insert(lst[t], logit, (int)v, tk, lane);
       }
     }
     cur = nxt;
+    sc_cur = sc_nxt;
     v = vn;
   }
 
-  // block merge per token: the warps' lists -> shared memory -> warp 0 selects the block's
-  // top-tk among the entries not worse than the best of the warps' tk-th entries
-  for (int t = 0; t < M; ++t) {
-    float lv = -INFINITY, thv = -INFINITY;
-    int li = 0x7fffffff, thi = 0x7fffffff;
+  // block merge: every warp writes its lists; warp t merges token t (threshold = best of
+  // the warps' tk-th entries, so at least tk entries survive)
+  __syncthreads();                          // xs is dead from here on: its bytes hold the lists
 #pragma unroll
-    for (int u = 0; u < MAXM; ++u)
-      if (u == t) { lv = lst[u].v; li = lst[u].i; thv = lst[u].thr_v; thi = lst[u].thr_i; }
-    mv[warp * kMaxTK + lane] = lv;
-    mi[warp * kMaxTK + lane] = li;
-    if (lane == 0) { th_v[warp] = thv; th_i[warp] = thi; }
-    __syncthreads();
-    if (warp == 0) {
-      float tv = lane < kWarps ? th_v[lane] : -INFINITY;
-      int ti = lane < kWarps ? th_i[lane] : 0x7fffffff;
-      warp_argmax(tv, ti);
-      auto ld = [&](int k, float& v, int& i) { v = mv[k]; i = mi[k]; };
-      warp_topk(ld, kWarps * kMaxTK, tk, tv, ti, tv_s, ti_s, kMergeCap, ov_s, oi_s, lane);
-      const size_t o = ((size_t)blockIdx.x * M + t) * tk;
-      for (int r = lane; r < tk; r += 32) { p.cand_val[o + r] = ov_s[r]; p.cand_idx[o + r] = oi_s[r]; }
+  for (int t = 0; t < MAXM; ++t) {
+    if (t < M) {
+      mv[(t * kWarps + warp) * kMaxTK + lane] = lst[t].v;
+      mi[(t * kWarps + warp) * kMaxTK + lane] = lst[t].i;
     }
-    __syncthreads();
+  }
+  __syncthreads();
+  for (int t = warp; t < M; t += kWarps) {
+    float tv = -INFINITY;
+    int ti = 0x7fffffff;
+    if (lane < kWarps) {
+      tv = mv[(t * kWarps + lane) * kMaxTK + tk - 1];
+      ti = mi[(t * kWarps + lane) * kMaxTK + tk - 1];
+    }
+    warp_argmax(tv, ti);
+    const float* lv = mv + t * kWarps * kMaxTK;
+    const int* li = mi + t * kWarps * kMaxTK;
+    auto ld = [&](int k, float& vv, int& ii) { vv = lv[k]; ii = li[k]; };
+    float* outv = ov + t * kMaxTK;
+    int* outi = oi + t * kMaxTK;
+    warp_topk(ld, kWarps * kMaxTK, tk, tv, ti, tv_s + warp * kMergeCap, ti_s + warp * kMergeCap, kMergeCap,
+              outv, outi, lane);
+    const size_t o = ((size_t)blockIdx.x * M + t) * tk;
+    for (int r = lane; r < tk; r += 32) { p.cand_val[o + r] = outv[r]; p.cand_idx[o + r] = outi[r]; }
   }
 
   // the last block to finish merges all blocks' candidates
@@ -302,26 +364,71 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
+  const int n = (int)(G * tk);
+  auto cand = [&](int t, int k, float& vv, int& ii) {
+    const size_t o = ((size_t)(k / tk) * M + t) * tk + (k % tk);
+    vv = ld_cg_f32(p.cand_val + o);
+    ii = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(p.cand_idx + o)));
+  };
+  // A. per token, the tk-th best of the blocks' first entries: tk distinct entries are not
+  //    worse than it, so it bounds the global tk-th entry from below
   for (int t = warp; t < M; t += kWarps) {
-    // threshold: the best of the blocks' tk-th entries
-    float tv = -INFINITY;
-    int ti = 0x7fffffff;
-    for (long long b = lane; b < G; b += 32) {
-      const size_t o = ((size_t)b * M + t) * tk + (tk - 1);
-      const float cv = ld_cg_f32(p.cand_val + o);
-      const int ci = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(p.cand_idx + o)));
-      if (beats(cv, ci, tv, ti)) { tv = cv; ti = ci; }
+    constexpr int PER = kMaxHeadGrid / 32;
+    float fv[PER];
+    int fi[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {                       // one load per block, all in flight
+      const int b = lane + 32 * j;
+      fv[j] = -INFINITY;
+      fi[j] = 0x7fffffff;
+      if (b < G) cand(t, b * tk, fv[j], fi[j]);
     }
-    warp_argmax(tv, ti);
-    auto ld = [&](int k, float& v, int& i) {
-      const size_t o = ((size_t)(k / tk) * M + t) * tk + (k % tk);
-      v = ld_cg_f32(p.cand_val + o);
-      i = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(p.cand_idx + o)));
-    };
-    float* outv = ov_s + warp * kMaxTK;
-    int* outi = oi_s + warp * kMaxTK;
-    warp_topk(ld, (int)(G * tk), tk, tv, ti, tv_s + warp * kMergeCap, ti_s + warp * kMergeCap,
-              kMergeCap, outv, outi, lane);
+    float kv;
+    int ki;
+    warp_kth<PER>(fv, fi, tk, kv, ki);
+    if (lane == 0) { thv[t] = kv; thi[t] = ki; cnt[t] = 0; }
+  }
+  __syncthreads();
+  // B. all threads: compact the candidates not worse than their token's threshold
+  float* cv_s = xs;                                        // reuse (lists are dead): [M][kMergeCap]
+  int* ci_s = reinterpret_cast<int*>(xs + (size_t)M * kMergeCap);
+  constexpr int kScan = 8;                                 // loads in flight per thread
+  for (int e0 = 0; e0 < M * n; e0 += blockDim.x * kScan) {
+    float vv[kScan];
+    int ii[kScan];
+#pragma unroll
+    for (int u = 0; u < kScan; ++u) {
+      const int e = e0 + u * blockDim.x + threadIdx.x;
+      vv[u] = -INFINITY;
+      ii[u] = 0x7fffffff;
+      if (e < M * n) cand(e / n, e % n, vv[u], ii[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kScan; ++u) {
+      const int e = e0 + u * blockDim.x + threadIdx.x;
+      if (e < M * n) {
+        const int t = e / n;
+        if (!beats(thv[t], thi[t], vv[u], ii[u])) {
+          const int pos = atomicAdd(&cnt[t], 1);
+          if (pos < kMergeCap) { cv_s[t * kMergeCap + pos] = vv[u]; ci_s[t * kMergeCap + pos] = ii[u]; }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // C. warp t selects token t's top-tk (rescans global memory only on a compaction overflow)
+  for (int t = warp; t < M; t += kWarps) {
+    float* outv = ov + t * kMaxTK;
+    int* outi = oi + t * kMaxTK;
+    if (cnt[t] <= kMergeCap) {
+      auto ld = [&](int k, float& vv, int& ii) { vv = cv_s[t * kMergeCap + k]; ii = ci_s[t * kMergeCap + k]; };
+      warp_topk(ld, cnt[t], tk, thv[t], thi[t], tv_s + warp * kMergeCap, ti_s + warp * kMergeCap, kMergeCap,
+                outv, outi, lane);
+    } else {
+      auto ld = [&](int k, float& vv, int& ii) { cand(t, k, vv, ii); };
+      warp_topk(ld, n, tk, thv[t], thi[t], tv_s + warp * kMergeCap, ti_s + warp * kMergeCap, kMergeCap,
+                outv, outi, lane);
+    }
     for (int r = lane; r < tk; r += 32) {
       if (r == 0) p.argmax_out[t] = outi[0];
       if (p.topk_idx) p.topk_idx[(size_t)t * tk + r] = outi[r];
@@ -332,7 +439,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
 
 template <bool FP8, int MAXM>
 cudaError_t launch_head_t(const HeadParams& p, cudaStream_t s) {
-  const size_t smem = head_smem_bytes(p.M);
+  const size_t smem = head_smem_bytes(p.M, MAXM);
   auto kern = head_kernel<FP8, MAXM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -38,26 +38,64 @@ namespace {
 constexpr int kRows13 = 2 * kI;                 // w13 rows per expert
 constexpr int kW13RowBytes = kH / 2;            // 1280
 constexpr int kW2RowBytes = kI / 2;             // 384
-constexpr int kXhBytes = kH * 2;                // f16 x-hat per token (planes layout)
-constexpr int kHhBytes = kI * 2;                // f16 h-hat per pair (planes layout)
-constexpr int kPairChunk = 48;                  // pairs quantised into smem at a time
+constexpr int kXhBytes = kH * 2 + 64;           // f16 x-hat per token, padded (conflict-free B loads)
+constexpr int kGuRound = 4 * kWarps;            // gate/up units per round (partials in smem)
+constexpr int kGuMaxTiles = 320;                // (tile, token-tile) entries per block
+constexpr int kTopkCand = 128;                  // compacted top-k candidates per warp
+constexpr int kHhBytes = kI * 2 + 64;           // f16 h-hat per pair, padded (conflict-free A loads)
+constexpr int kPairChunk = 24;                  // pairs quantised into smem at a time
+// per-warp cp.async rings (16-byte asynchronous copies into padded, bank-conflict-free rows)
+constexpr int kGuU = 8;                         // gate/up: 32-blocks per stage
+constexpr int kGuStages = 3;
+constexpr int kGuPitch = kGuU * 16 + 16;        // bytes per staged row (16 rows per stage)
+constexpr int kGuStageBytes = 16 * kGuPitch + 16 * kGuU;
+constexpr int kDnStages = 2;                    // down: 16 W2 rows x 12 blocks per stage
+constexpr int kDnKB = kIBlocks / 2;             // blocks per K half (12)
+constexpr int kDnPitch = kDnKB * 16 + 16;       // 208 bytes: conflict-free fragment reads
+constexpr int kDnStageBytes = 16 * kDnPitch + 16 * kIBlocks;
+constexpr int kWarpRing = (kGuStages * kGuStageBytes > kDnStages * kDnStageBytes)
+                              ? kGuStages * kGuStageBytes : kDnStages * kDnStageBytes;
 constexpr int kMaxRowsPerBlock = 32;            // down-projection rows per block (>= H / grid)
+
+// ------------------------------------------------------------------ phase trace
+
+// Built only with -DMDW_TRACE (a profiling build of the library, never the product build):
+// thread 0 of every block records %globaltimer at each phase boundary of every layer.
+#ifdef MDW_TRACE
+constexpr int kTracePhases = 16;
+constexpr int kTraceLayers = 64;
+__device__ unsigned long long g_trace[kTraceLayers * kTracePhases * 256];
+#define MDW_TRACE_POINT(layer, phase)                                                        \
+  do {                                                                                       \
+    if (threadIdx.x == 0 && (layer) < kTraceLayers) {                                        \
+      unsigned long long t_;                                                                 \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                 \
+      g_trace[((layer) * kTracePhases + (phase)) * 256 + blockIdx.x] = t_;                   \
+    }                                                                                        \
+  } while (0)
+#else
+#define MDW_TRACE_POINT(layer, phase) do { } while (0)
+#endif
 
 // Shared-memory carve-up (bytes), for M tokens.
 struct Smem {
-  size_t xh, xb, hh, part, yacc, small, total;
+  size_t xh, xb, hh, ring, part, yacc, gured, small, total;
 };
+// R1 = x-hat (gate/up) or h-hat (down); R2 = bf16 x (router) or the per-warp cp.async rings.
 __host__ __device__ inline Smem smem_layout(int M) {
   Smem s;
+  const size_t r1 = (size_t)M * kXhBytes > (size_t)kPairChunk * kHhBytes ? (size_t)M * kXhBytes
+                                                                          : (size_t)kPairChunk * kHhBytes;
+  const size_t r2 = (size_t)M * kH * 2 > (size_t)kWarps * kWarpRing ? (size_t)M * kH * 2
+                                                                     : (size_t)kWarps * kWarpRing;
   s.xh = 0;
-  s.xb = s.xh + (size_t)M * kXhBytes;
-  size_t region = s.xb + (size_t)M * kH * 2;                   // x-hat + bf16 x
-  size_t hh_bytes = (size_t)kPairChunk * kHhBytes;             // reuses the x region
   s.hh = 0;
-  size_t big = region > hh_bytes ? region : hh_bytes;
-  s.part = (big + 15) & ~(size_t)15;                            // [kPairChunk][rows] fp32
+  s.xb = (r1 + 127) & ~(size_t)127;
+  s.ring = s.xb;
+  s.part = (s.xb + r2 + 15) & ~(size_t)15;                      // [kPairChunk][rows] fp32
   s.yacc = s.part + (size_t)kPairChunk * kMaxRowsPerBlock * 4;     // [M][rows] fp32
-  s.small = s.yacc + (size_t)M * kMaxRowsPerBlock * 4;
+  s.gured = s.yacc + (size_t)M * kMaxRowsPerBlock * 4;               // [kGuRound][32][4] fp32
+  s.small = s.gured + (size_t)kGuRound * 32 * 4 * 4;   // also holds the routing candidates
   s.total = s.small + 12288;
   return s;
 }
@@ -76,8 +114,12 @@ struct Tables {
   int cnt[MDW_MAX_M * MDW_MAX_TOPK + 1];
   float sx[MDW_MAX_M];
   float inv_rms[MDW_MAX_M];
+  float part[MDW_MAX_M * (kH / 256)];          // per-(token, 32-chunk group) partials
+  float cand_g[MDW_MAX_M * MDW_MAX_TOPK];      // gates before they replace the logits
   float sh[kPairChunk];
   int n_slots, n_routed, n_pairs, shared_slot, bad;
+  int gu_n;                                    // entries in gu_tile
+  int4 gu_tile[kGuMaxTiles];                   // (slot, j0, rows, first token column)
 };
 static_assert(sizeof(Tables) <= 12288, "tables exceed the reserved shared memory");
 
@@ -90,72 +132,86 @@ __device__ __forceinline__ const __nv_bfloat16* resid_ptr(const MoeParams& p, in
   return p.resid + (size_t)slot * p.M * kH;
 }
 
-// x-hat planes layout: token t, block b, plane c (elements 8c..8c+7 of the block) at
-// byte t*kXhBytes + (c*kHBlocks + b)*16.
+// x-hat layout: token t's f16 values in natural order at byte t*kXhBytes (+64 B padding per
+// token, so the 8 token rows of an MMA B fragment fall in distinct banks).
 template <int MAXM>
 __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tables& tb) {
   const int M = p.M;
+  constexpr int CPT = kH / 8;                 // 16-byte chunks per token (320, a multiple of 32)
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(smem + smem_layout(M).xb);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const __nv_bfloat16* src = !p.stack_mode ? p.x_in : resid_ptr(p, layer);
-  // 1. copy (stack: then normalise) into xb; one warp per token
-  for (int t = warp; t < M; t += kWarps) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)t * kH);
-    uint4* d4 = reinterpret_cast<uint4*>(xb + (size_t)t * kH);
-    if (!p.stack_mode) {
-      for (int i = lane; i < kH / 8; i += 32) d4[i] = ld_cg16(s4 + i);
-    } else {
-      float ss = 0.f;
-      for (int i = lane; i < kH / 8; i += 32) {
-        uint4 v = ld_cg16(s4 + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint4* xb4 = reinterpret_cast<uint4*>(xb);
+  const int lane = threadIdx.x & 31;
+  const uint4* src = reinterpret_cast<const uint4*>(!p.stack_mode ? p.x_in : resid_ptr(p, layer));
+  // Every block must derive bit-identical x and xq: per-token reductions are taken in a fixed
+  // order (a warp's 32 chunks share one token; the 10 warp partials are summed in order).
+  // 1. load (all threads, one 16-byte chunk each); stack: sum of squares, else: amax
+  for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
+    const uint4 v = ld_cg16(src + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float r = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float a = __uint_as_float(w[k] << 16), b = __uint_as_float(w[k] & 0xFFFF0000u);
-          ss = fmaf(a, a, ss);
-          ss = fmaf(b, b, ss);
-        }
-        d4[i] = v;
-      }
-      ss = warp_sum(ss);
-      const float inv = rsqrtf(ss / (float)kH + 1e-6f);
-      for (int i = lane; i < kH / 8; i += 32) {
-        uint4 v = d4[i];
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float a = __uint_as_float(w[k] << 16) * inv, b = __uint_as_float(w[k] & 0xFFFF0000u) * inv;
-          __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-          w[k] = *reinterpret_cast<uint32_t*>(&r);
-        }
-        d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float a = __uint_as_float(w[k] << 16), b = __uint_as_float(w[k] & 0xFFFF0000u);
+      if (p.stack_mode) { r = fmaf(a, a, r); r = fmaf(b, b, r); }
+      else r = fmaxf(r, fmaxf(fabsf(a), fabsf(b)));
     }
+    r = p.stack_mode ? warp_sum(r) : warp_max(r);
+    if (lane == 0) tb.part[c / 32] = r;
+    xb4[c] = v;
   }
   __syncthreads();
-  // 2. per-token E4M3 quantisation: amax exact, scale = amax/448 and x/scale correctly
-  //    rounded (IEEE division), round-to-nearest-even saturating conversion
-  for (int t = warp; t < M; t += kWarps) {
-    const uint32_t* x32 = reinterpret_cast<const uint32_t*>(xb + (size_t)t * kH);
+  if (p.stack_mode) {
+    // 2. x = bf16(r * rsqrt(mean(r^2) + eps)), then its amax
+    if (threadIdx.x < M) {
+      float ss = 0.f;
+      for (int g = 0; g < CPT / 32; ++g) ss += tb.part[threadIdx.x * (CPT / 32) + g];
+      tb.inv_rms[threadIdx.x] = rsqrtf(ss / (float)kH + 1e-6f);
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
+      const float inv = tb.inv_rms[c / CPT];
+      const uint4 v = xb4[c];
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float am = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 r2 = __floats2bfloat162_rn(__uint_as_float(w[k] << 16) * inv,
+                                                        __uint_as_float(w[k] & 0xFFFF0000u) * inv);
+        w[k] = *reinterpret_cast<const uint32_t*>(&r2);
+        am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
+      }
+      am = warp_max(am);
+      if (lane == 0) tb.part[c / 32] = am;
+      xb4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+  }
+  // 3. per-token scale = amax/448 (IEEE division), then codes: x/scale correctly rounded,
+  //    round-to-nearest-even saturating conversion; x-hat (f16) into the planes layout
+  if (threadIdx.x < M) {
     float am = 0.f;
-    for (int i = lane; i < kH / 2; i += 32) {
-      uint32_t w = x32[i];
-      am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xFFFF0000u))));
+    for (int g = 0; g < CPT / 32; ++g) am = fmaxf(am, tb.part[threadIdx.x * (CPT / 32) + g]);
+    const float sc = am > 0.f ? __fdiv_rn(am, kE4M3Max) : 1.0f;
+    tb.sx[threadIdx.x] = sc;
+    if (blockIdx.x == 0) p.sx[threadIdx.x] = sc;
+  }
+  __syncthreads();
+  const bool writer = (blockIdx.x == 0);
+  for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
+    const int t = c / CPT, i = c % CPT;           // chunk i = elements 8i .. 8i+7 of token t
+    const float sc = tb.sx[t];
+    const uint4 v = xb4[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t q[4], h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      q[k] = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[k] << 16), sc),
+                             __fdiv_rn(__uint_as_float(w[k] & 0xFFFF0000u), sc));
+      h[k] = e4m3x2_to_f16x2(q[k]);
     }
-    am = warp_max(am);
-    const float s = am > 0.f ? __fdiv_rn(am, kE4M3Max) : 1.0f;
-    if (lane == 0) tb.sx[t] = s;
-    uint8_t* xh = smem + (size_t)t * kXhBytes;
-    const bool writer = (blockIdx.x == 0);
-    for (int i = lane; i < kH / 2; i += 32) {      // element pair (2i, 2i+1)
-      uint32_t w = x32[i];
-      uint32_t q = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w << 16), s),
-                                   __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
-      const int e = 2 * i, b = e >> 5, c = (e & 31) >> 3, o = e & 7;
-      *reinterpret_cast<uint32_t*>(xh + (size_t)(c * kHBlocks + b) * 16 + o * 2) = e4m3x2_to_f16x2(q);
-      if (writer) reinterpret_cast<uint16_t*>(p.xq + (size_t)t * kH)[i] = (uint16_t)q;
-    }
-    if (writer && lane == 0) p.sx[t] = s;
+    *reinterpret_cast<uint4*>(smem + (size_t)t * kXhBytes + (size_t)i * 16) = make_uint4(h[0], h[1], h[2], h[3]);
+    if (writer)
+      reinterpret_cast<uint2*>(p.xq + (size_t)t * kH)[i] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
   }
   __syncthreads();
 }
@@ -194,15 +250,14 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
 
 // ------------------------------------------------------------------ P2: top-k + dedup
 
-__device__ void route_tokens(const MoeParams& p, Tables& tb, int layer) {
+__device__ void route_tokens(const MoeParams& p, Tables& tb, int layer, uint8_t* scratch) {
   const int M = p.M, E = p.E, K = p.K;
+  // per-warp candidate buffers live in the gate/up partial-sum region (not live during
+  // routing)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < MDW_MAX_EXPERTS / 32) tb.bitmap[threadIdx.x] = 0;
   if (threadIdx.x == 0) tb.bad = 0;
-  __syncthreads();
-  for (int t = warp; t < M; t += kWarps) {
-    const float* z = p.logits + (size_t)t * E;
-    if (p.topk_override) {
+  if (p.topk_override) {
+    for (int t = warp; t < M; t += kWarps) {
       if (lane < K) {
         int id = p.topk_override[t * K + lane];
         bool ok = id >= 0 && id < E;
@@ -210,125 +265,169 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb, int layer) {
           if (j != lane && p.topk_override[t * K + j] == id) ok = false;
         if (!ok) { atomicExch(&tb.bad, 1); id = 0; }
         tb.ids[t * K + lane] = id;
-        tb.gts[t * K + lane] = ld_cg_f32(z + id);
+        tb.gts[t * K + lane] = ld_cg_f32(p.logits + (size_t)t * E + id);
       }
-      __syncwarp();
-    } else {
-      // k rounds of warp arg-max over E logits (16 per lane), ties -> lower index
-      float v[MDW_MAX_EXPERTS / 32];
-      const int per = (E + 31) / 32;
-#pragma unroll
-      for (int i = 0; i < MDW_MAX_EXPERTS / 32; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = (i < per && e < E) ? ld_cg_f32(z + e) : -INFINITY;
-      }
-      for (int r = 0; r < K; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < MDW_MAX_EXPERTS / 32; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && beats(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
-        }
-        warp_argmax(bv, bi);
-        if ((bi & 31) == lane) {
-#pragma unroll
-          for (int i = 0; i < MDW_MAX_EXPERTS / 32; ++i)
-            if (lane + 32 * i == bi) v[i] = -INFINITY;
-        }
-        if (lane == 0) { tb.ids[t * K + r] = bi; tb.gts[t * K + r] = bv; }
-      }
-      __syncwarp();
     }
-    // gates: softmax over the selected logits
-    if (lane == 0) {
-      float mx = -INFINITY;
-      for (int r = 0; r < K; ++r) mx = fmaxf(mx, tb.gts[t * K + r]);
-      float sum = 0.f;
-      float ex[MDW_MAX_TOPK];
-      for (int r = 0; r < K; ++r) { ex[r] = expf(tb.gts[t * K + r] - mx); sum += ex[r]; }
-      for (int r = 0; r < K; ++r) tb.gts[t * K + r] = ex[r] / sum;
+  } else {
+    // Top-K per token, one warp per token (ties -> lower expert id):
+    //  1. each lane holds E/32 logits and its local best;
+    //  2. a bitonic sort of the 32 lane bests across the warp; T = the K-th of them. K
+    //     distinct logits are not worse than T, so T bounds the K-th largest from below;
+    //  3. the logits not worse than T (typically little more than K) are compacted into
+    //     shared memory and ranked among themselves; rank < K gives the result in order.
+    float* cv_all = reinterpret_cast<float*>(scratch);
+    int* ci_all = reinterpret_cast<int*>(cv_all + kWarps * kTopkCand);
+    int* cnt_all = ci_all + kWarps * kTopkCand;
+    for (int t = warp; t < M; t += kWarps) {
+      const float* z = p.logits + (size_t)t * E;
+      constexpr int PER = MDW_MAX_EXPERTS / 32;
+      float v[PER];
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? ld_cg_f32(z + e) : -INFINITY;
+        if (e < E && beats(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
+      }
+      // bitonic sort of (bv, bi), descending in `beats` order
+#pragma unroll
+      for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, jj);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, jj);
+          const bool up = ((lane & kk) == 0);              // this pair sorts descending
+          const bool lower = ((lane & jj) == 0);
+          const bool take_better = (up == lower);
+          const bool o_better = beats(ov, oi, bv, bi);
+          if (take_better ? o_better : !o_better && !(ov == bv && oi == bi)) { bv = ov; bi = oi; }
+        }
+      const float tv = __shfl_sync(0xffffffffu, bv, K - 1);
+      const int ti = __shfl_sync(0xffffffffu, bi, K - 1);
+      float* cv = cv_all + warp * kTopkCand;
+      int* ci = ci_all + warp * kTopkCand;
+      int count = 0;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int e = lane + 32 * j;
+        const bool keep = e < E && !beats(tv, ti, v[j], e);
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        const int pos = count + __popc(m & ((1u << lane) - 1u));
+        if (keep && pos < kTopkCand) { cv[pos] = v[j]; ci[pos] = e; }
+        count += __popc(m);
+      }
+      __syncwarp();
+      if (lane == 0) cnt_all[warp] = count;
+      if (count <= kTopkCand) {
+        for (int k = lane; k < count; k += 32) {
+          const float vv = cv[k];
+          const int ii = ci[k];
+          int rank = 0;
+          for (int o = 0; o < count; ++o) rank += beats(cv[o], ci[o], vv, ii);
+          if (rank < K) { tb.ids[t * K + rank] = ii; tb.gts[t * K + rank] = vv; }
+        }
+      } else {
+        // many equal logits: K rounds of warp arg-max over the register-held logits
+        float pv = INFINITY;
+        int pi = -1;
+        for (int r = 0; r < K; ++r) {
+          float best = -INFINITY;
+          int bidx = 0x7fffffff;
+#pragma unroll
+          for (int j = 0; j < PER; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && beats(pv, pi, v[j], e) && beats(v[j], e, best, bidx)) { best = v[j]; bidx = e; }
+          }
+          warp_argmax(best, bidx);
+          pv = best; pi = bidx;
+          if (lane == 0) { tb.ids[t * K + r] = bidx; tb.gts[t * K + r] = best; }
+        }
+      }
+      __syncwarp();
     }
   }
   __syncthreads();
+  MDW_TRACE_POINT(layer, 10);
   if (tb.bad) return;
-  // union bitmap
-  for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
-    const int id = tb.ids[i];
-    atomicOr(&tb.bitmap[id >> 5], 1u << (id & 31));
-  }
-  __syncthreads();
-  const int first = p.has_shared ? 1 : 0;
+  // Routing tables, built by warp 0 alone: gates, the union of the selections, slots
+  // (slot 0 = shared expert when present, then the union ascending) and the pairs
+  // (slot-major, token-minor).
   if (warp == 0) {
-    // slot 0 = shared expert (if any), then the routed union ascending
+    // gates: softmax over each token's selected logits, one (token, rank) per lane
+    for (int i = lane; i < M * K; i += 32) {
+      const int t = i / K;
+      const float* z = tb.gts + t * K;
+      float mx = z[0];
+      for (int r = 1; r < K; ++r) mx = fmaxf(mx, z[r]);
+      float sum = 0.f;
+      for (int r = 0; r < K; ++r) sum += expf(z[r] - mx);
+      tb.cand_g[i] = expf(z[i % K] - mx) / sum;
+    }
+    __syncwarp();
+    for (int i = lane; i < M * K; i += 32) tb.gts[i] = tb.cand_g[i];
+    if (lane < MDW_MAX_EXPERTS / 32) tb.bitmap[lane] = 0;
+    __syncwarp();
+    for (int i = lane; i < M * K; i += 32) atomicOr(&tb.bitmap[tb.ids[i] >> 5], 1u << (tb.ids[i] & 31));
+    __syncwarp();
+    const int first = p.has_shared ? 1 : 0;
     const uint32_t word = lane < MDW_MAX_EXPERTS / 32 ? tb.bitmap[lane] : 0u;
     int cnt = __popc(word), incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
+      const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += nb;
     }
     if (lane < MDW_MAX_EXPERTS / 32) tb.wpre[lane] = incl - cnt;
     int pos = first + incl - cnt;
-    uint32_t w = word;
-    while (w) {
-      const int b = __ffs(w) - 1;
-      w &= w - 1;
+    for (uint32_t w = word; w; w &= w - 1) {
       tb.cnt[pos] = 0;
-      tb.slot_expert[pos++] = lane * 32 + b;
+      tb.slot_expert[pos++] = lane * 32 + __ffs(w) - 1;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int S = total + first;
     if (lane == 0) {
       tb.n_routed = total;
-      tb.n_slots = total + first;
-      if (p.has_shared) { tb.slot_expert[0] = -1; tb.cnt[0] = M; }
+      tb.n_slots = S;
       tb.shared_slot = p.has_shared ? 0 : -1;
+      if (p.has_shared) { tb.slot_expert[0] = -1; tb.cnt[0] = M; }
     }
-  }
-  __syncthreads();
-  auto slot_of = [&](int e) {
-    return first + tb.wpre[e >> 5] + __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-  };
-  for (int i = threadIdx.x; i < M * K; i += blockDim.x) atomicAdd(&tb.cnt[slot_of(tb.ids[i])], 1);
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the per-slot pair counts (S <= 257)
-    const int S = tb.n_slots;
+    __syncwarp();
+    auto slot_of = [&](int e) {
+      return first + tb.wpre[e >> 5] + __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
+    };
+    for (int i = lane; i < M * K; i += 32) atomicAdd(&tb.cnt[slot_of(tb.ids[i])], 1);
+    __syncwarp();
     int carry = 0;
     for (int b0 = 0; b0 < S; b0 += 32) {
-      const int s = b0 + lane;
-      const int c = s < S ? tb.cnt[s] : 0;
-      int incl = c;
+      const int sidx = b0 + lane;
+      const int c = sidx < S ? tb.cnt[sidx] : 0;
+      int in2 = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+        const int nb = __shfl_up_sync(0xffffffffu, in2, o);
+        if (lane >= o) in2 += nb;
       }
-      if (s < S) tb.slot_begin[s] = carry + incl - c;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (sidx < S) tb.slot_begin[sidx] = carry + in2 - c;
+      carry += __shfl_sync(0xffffffffu, in2, 31);
     }
     if (lane == 0) { tb.slot_begin[S] = carry; tb.n_pairs = carry; }
-  }
-  __syncthreads();
-  // pair of (t, r): slot-major, token-minor
-  for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
-    const int t = i / K, e = tb.ids[i];
-    int rank = 0;
-    for (int t2 = 0; t2 < t; ++t2)
-      for (int r2 = 0; r2 < K; ++r2) rank += (tb.ids[t2 * K + r2] == e);
-    const int s = slot_of(e);
-    const int q = tb.slot_begin[s] + rank;
-    tb.pair_token[q] = t;
-    tb.pair_slot[q] = s;
-    tb.pair_gate[q] = tb.gts[i];
-  }
-  if (p.has_shared)
-    for (int t = threadIdx.x; t < M; t += blockDim.x) {
-      tb.pair_token[t] = t;
-      tb.pair_slot[t] = 0;
-      tb.pair_gate[t] = 1.0f;
+    __syncwarp();
+    for (int i = lane; i < M * K; i += 32) {
+      const int t = i / K, e = tb.ids[i];
+      int rank = 0;
+      for (int t2 = 0; t2 < t; ++t2)
+        for (int r2 = 0; r2 < K; ++r2) rank += (tb.ids[t2 * K + r2] == e);
+      const int sidx = slot_of(e), q = tb.slot_begin[sidx] + rank;
+      tb.pair_token[q] = t;
+      tb.pair_slot[q] = sidx;
+      tb.pair_gate[q] = tb.gts[i];
     }
+    if (p.has_shared)
+      for (int t = lane; t < M; t += 32) { tb.pair_token[t] = t; tb.pair_slot[t] = 0; tb.pair_gate[t] = 1.0f; }
+  }
   __syncthreads();
+  MDW_TRACE_POINT(layer, 11);
   if (blockIdx.x == 0) {
     // publish the routing (inspection + optional outputs)
     for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
@@ -354,126 +453,187 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb, int layer) {
 
 // ------------------------------------------------------------------ P3: gate/up + SwiGLU
 
-// One warp computes gate_j and up_j of one expert for the tokens of one slot and writes
-// h = silu(gate) * up. Lane l reads (16-byte chunks = one MX block each): gate blocks l,
-// l+32; up blocks l, l+32; and block 64 + (l & 15) of gate (l < 16) or up (l >= 16).
-template <int MAXM>
-struct RowPairLoad {
-  uint4 q[5];
-  uint32_t s[5];
-};
-
-__device__ __forceinline__ int rp_block(int c, int lane) {
-  return c < 4 ? (lane + 32 * (c & 1)) : 64 + (lane & 15);
+// D += A x B on the tensor cores: m16n8k16, f16 operands (exact for E2M1 and E4M3 values),
+// fp32 accumulation.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ bool rp_is_up(int c, int lane) {
-  return c < 4 ? (c >= 2) : (lane >= 16);
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(d), "l"(src) : "memory");
 }
-
-template <int MAXM>
-__device__ __forceinline__ void rp_load(RowPairLoad<MAXM>& ld, const uint8_t* q13, const uint8_t* s13,
-                                        int j, int lane) {
-#pragma unroll
-  for (int c = 0; c < 5; ++c) {
-    const int row = j + (rp_is_up(c, lane) ? kI : 0);
-    const int b = rp_block(c, lane);
-    ld.q[c] = ldg_stream16(q13 + (size_t)row * kW13RowBytes + b * 16);
-    ld.s[c] = ldg_stream_u8(s13 + (size_t)row * kHBlocks + b);
-  }
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(d), "l"(src) : "memory");
 }
-
-template <int MAXM>
-__device__ __forceinline__ void rp_compute(const RowPairLoad<MAXM>& ld, const uint8_t* smem,
-                                           const uint32_t (&xr)[3][16], const int* toks, int m,
-                                           const float* sx, float* hout /* h[pair0][j], stride kI */,
-                                           int lane) {
-  float g[MAXM], u[MAXM];
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// One MMA tile of the gate/up GEMVs: rows 0..7 of the MMA = gate rows j0..j0+7 and rows
+// 8..15 = the matching up rows of one expert; columns = 8 tokens of the slot; K = blocks
+// [kb0, kb1) of 32 (a multiple of kGuU). The weight rows stream through the warp's
+// cp.async ring (kGuStages stages of kGuU blocks x 16 rows, rows padded so the fragment
+// reads are bank-conflict free). Each 32-block is two k16 MMAs on a permuted K order: lane
+// (g, q) feeds bytes 4q..4q+3 of the block (E2M1 pairs, via cvt.e2m1x2) as its A registers
+// and the matching x-hat values 8q..8q+7 (one 16-byte load) as its B registers; the block's
+// fresh fp32 result is scaled by its E8M0 scale (per row) into the accumulator:
+//   acc[0..1] = gate rows g, tokens 2q..2q+1;  acc[2..3] = up rows g, same tokens.
+__device__ __forceinline__ void gate_up_tile(const uint8_t* q13, const uint8_t* s13, int j0, int nr,
+                                             const uint8_t* xtok, int kb0, int kb1, float (&acc)[4],
+                                             uint8_t* ring, int lane) {
+  const int g = lane >> 2, q = lane & 3;
+  const bool rv = g < nr;
+  const int nst = (kb1 - kb0) / kGuU;
+  auto issue = [&](int st) {
+    uint8_t* dst = ring + (st % kGuStages) * kGuStageBytes;
+    const int bb = kb0 + st * kGuU;
 #pragma unroll
-  for (int i = 0; i < MAXM; ++i) { g[i] = 0.f; u[i] = 0.f; }
-#pragma unroll
-  for (int c = 0; c < 5; ++c) {
-    uint32_t w2[16];
-    mx_block_decode(ld.q[c], w2);
-    const float sc = e8m0_to_f32(ld.s[c]);
-    const int b = rp_block(c, lane);
-    const bool up = rp_is_up(c, lane);
-    const int xi = c < 4 ? (c & 1) : 2;
-#pragma unroll
-    for (int i = 0; i < MAXM; ++i) {
-      if (i < m) {
-        float d;
-        if (MAXM == 1) {
-          d = dot32_f16(w2, xr[xi]);
-        } else {
-          const uint8_t* xh = smem + (size_t)toks[i] * kXhBytes;
-          uint32_t x2[16];
-#pragma unroll
-          for (int pl = 0; pl < 4; ++pl) {
-            uint4 v = *reinterpret_cast<const uint4*>(xh + (size_t)(pl * kHBlocks + b) * 16);
-            x2[4 * pl] = v.x; x2[4 * pl + 1] = v.y; x2[4 * pl + 2] = v.z; x2[4 * pl + 3] = v.w;
-          }
-          d = dot32_f16(w2, x2);
-        }
-        if (up) u[i] = fmaf(d, sc, u[i]); else g[i] = fmaf(d, sc, g[i]);
+    for (int k = 0; k < 16 * kGuU / 32; ++k) {        // 16 rows x kGuU chunks of 16 bytes
+      const int c = lane + 32 * k, row = c / kGuU, blk = c % kGuU, rr = row & 7;
+      if (rr < nr) {
+        const size_t grow = (size_t)(row < 8 ? j0 + rr : kI + j0 + rr);
+        cp_async16(dst + row * kGuPitch + blk * 16, q13 + grow * kW13RowBytes + (bb + blk) * 16);
       }
     }
-  }
-#pragma unroll
-  for (int i = 0; i < MAXM; ++i) {
-    if (i < m) {
-      const float gs = warp_sum(g[i]) * sx[toks[i]];
-      const float us = warp_sum(u[i]) * sx[toks[i]];
-      if (lane == 0) hout[(size_t)i * kI] = gs / (1.0f + expf(-gs)) * us;
-    }
-  }
-}
-
-// Row pairs [r0, r1) of the virtual space; slot s covers [s*kI, (s+1)*kI).
-template <int MAXM>
-__device__ void gate_up_range(const MoeParams& p, const LayerDesc& L, const uint8_t* smem,
-                              const Tables& tb, int r0, int r1, int slot_offset) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t xr[3][16];
-  if (MAXM == 1) {
-    const int blocks[3] = {lane, lane + 32, 64 + (lane & 15)};
-#pragma unroll
-    for (int k = 0; k < 3; ++k)
-#pragma unroll
-      for (int pl = 0; pl < 4; ++pl) {
-        uint4 v = *reinterpret_cast<const uint4*>(smem + (size_t)(pl * kHBlocks + blocks[k]) * 16);
-        xr[k][4 * pl] = v.x; xr[k][4 * pl + 1] = v.y; xr[k][4 * pl + 2] = v.z; xr[k][4 * pl + 3] = v.w;
-      }
-  }
-  int rp = r0 + warp;
-  if (rp >= r1) return;
-  RowPairLoad<MAXM> cur, nxt;
-  auto expert_ptrs = [&](int vrp, const uint8_t*& q13, const uint8_t*& s13, int& j, int& slot) {
-    slot = vrp / kI + slot_offset;
-    j = vrp % kI;
-    const int e = tb.slot_expert[slot];
-    if (e < 0) { q13 = L.sh_w13_q; s13 = L.sh_w13_s; }
-    else {
-      q13 = L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
-      s13 = L.w13_s + (size_t)e * kRows13 * kHBlocks;
+    if (lane < 16 && (lane & 7) < nr) {                // 16 rows x kGuU scale bytes
+      const size_t grow = (size_t)(lane < 8 ? j0 + lane : kI + j0 + (lane & 7));
+      cp_async8(dst + 16 * kGuPitch + lane * 8, s13 + grow * kHBlocks + bb);
     }
   };
-  const uint8_t *q13, *s13;
-  int j, slot;
-  expert_ptrs(rp, q13, s13, j, slot);
-  rp_load<MAXM>(cur, q13, s13, j, lane);
-  while (true) {
-    const int nrp = rp + kWarps;
-    const uint8_t *nq13 = nullptr, *ns13 = nullptr;
-    int nj = 0, nslot = 0;
-    if (nrp < r1) {
-      expert_ptrs(nrp, nq13, ns13, nj, nslot);
-      rp_load<MAXM>(nxt, nq13, ns13, nj, lane);
+#pragma unroll
+  for (int st = 0; st < kGuStages - 1; ++st) {
+    if (st < nst) issue(st);
+    cp_async_commit();
+  }
+  for (int st = 0; st < nst; ++st) {
+    if (st + kGuStages - 1 < nst) issue(st + kGuStages - 1);
+    cp_async_commit();
+    cp_async_wait<kGuStages - 1>();
+    __syncwarp();
+    const uint8_t* buf = ring + (st % kGuStages) * kGuStageBytes;
+    const int bb = kb0 + st * kGuU;
+    uint2 scg = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu), scu = scg;
+    if (rv) {
+      scg = *reinterpret_cast<const uint2*>(buf + 16 * kGuPitch + g * 8);
+      scu = *reinterpret_cast<const uint2*>(buf + 16 * kGuPitch + (g + 8) * 8);
     }
-    const int pb = tb.slot_begin[slot], m = tb.slot_begin[slot + 1] - pb;
-    rp_compute<MAXM>(cur, smem, xr, tb.pair_token + pb, m, tb.sx, p.h + (size_t)pb * kI + j, lane);
-    if (nrp >= r1) break;
-    cur = nxt;
-    rp = nrp; j = nj; slot = nslot;
+#pragma unroll
+    for (int u = 0; u < kGuU; ++u) {
+      uint32_t wg = 0, wu = 0;
+      if (rv) {
+        wg = *reinterpret_cast<const uint32_t*>(buf + g * kGuPitch + u * 16 + 4 * q);
+        wu = *reinterpret_cast<const uint32_t*>(buf + (g + 8) * kGuPitch + u * 16 + 4 * q);
+      }
+      uint4 xv = make_uint4(0, 0, 0, 0);
+      if (xtok) xv = *reinterpret_cast<const uint4*>(xtok + 64 * (bb + u) + 16 * q);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816(d, e2m1x2_to_f16x2(wg & 0xFF), e2m1x2_to_f16x2(wu & 0xFF),
+                e2m1x2_to_f16x2((wg >> 8) & 0xFF), e2m1x2_to_f16x2((wu >> 8) & 0xFF), xv.x, xv.y);
+      mma_16816(d, e2m1x2_to_f16x2((wg >> 16) & 0xFF), e2m1x2_to_f16x2((wu >> 16) & 0xFF),
+                e2m1x2_to_f16x2(wg >> 24), e2m1x2_to_f16x2(wu >> 24), xv.z, xv.w);
+      const uint32_t sgw = u < 4 ? scg.x : scg.y, suw = u < 4 ? scu.x : scu.y;
+      const float fg = e8m0_to_f32((sgw >> (8 * (u & 3))) & 0xFF);
+      const float fu = e8m0_to_f32((suw >> (8 * (u & 3))) & 0xFF);
+      acc[0] = fmaf(fg, d[0], acc[0]);
+      acc[1] = fmaf(fg, d[1], acc[1]);
+      acc[2] = fmaf(fu, d[2], acc[2]);
+      acc[3] = fmaf(fu, d[3], acc[3]);
+    }
+    __syncwarp();
+  }
+}
+
+// Tile list of virtual row pairs [a, b) (slot s covers [s*kI, (s+1)*kI), slot_offset added):
+// tiles of up to 8 row pairs inside one slot, one entry per 8-token column group.
+__device__ void build_gate_up_tiles(const Tables& tb, int a, int b, int slot_offset, Tables& out) {
+  if (threadIdx.x == 0) {
+    int n = 0;
+    while (a < b && n < kGuMaxTiles) {
+      const int slot = a / kI + slot_offset, j0 = a % kI;
+      const int nr = min(8, min(kI - j0, b - a));
+      const int m = tb.slot_begin[slot + 1] - tb.slot_begin[slot];
+      for (int n0 = 0; n0 < m && n < kGuMaxTiles; n0 += 8) out.gu_tile[n++] = make_int4(slot, j0, nr, n0);
+      a += nr;
+    }
+    out.gu_n = n;
+  }
+  __syncthreads();
+}
+
+// All gate/up tiles of the block's list: units (tile, K half) in rounds of kGuRound; the two
+// halves' partials are summed in a fixed order, then SwiGLU, then h per (pair, row).
+__device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, Tables& tb,
+                              bool prefetch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  float4* red = reinterpret_cast<float4*>(const_cast<uint8_t*>(smem) + smem_layout(p.M).gured);
+  // K split per tile (a divisor of the 10 stages of 8 blocks): about one unit per warp when
+  // the block has few tiles, whole tiles (10 pipelined stages) when it has many
+  const int want = kWarps / max(1, tb.gu_n);
+  const int ks = want >= 10 ? 10 : want >= 5 ? 5 : want >= 2 ? 2 : 1;
+  const int units = tb.gu_n * ks;
+  const int kpart = kHBlocks / ks;
+  const int round = kGuRound / ks * ks;            // a whole number of tiles per round
+  for (int u0 = 0; u0 < units; u0 += round) {
+    const int un = min(round, units - u0);
+    // each warp's lane 0 first asks L2 for its own units' rows (bulk prefetches of the
+    // tile's 8 contiguous gate rows and 8 contiguous up rows, and their scales)
+    if (lane == 0 && prefetch) {
+      for (int u = warp; u < un; u += kWarps) {
+        const int4 t = tb.gu_tile[(u0 + u) / ks];
+        const int kp = (u0 + u) % ks;
+        const int e = tb.slot_expert[t.x];
+        const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
+        const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
+        if (kp == 0) {                   // the tile's first K part prefetches the whole tile
+          prefetch_l2(q13 + (size_t)t.y * kW13RowBytes, t.z * kW13RowBytes);
+          prefetch_l2(q13 + (size_t)(kI + t.y) * kW13RowBytes, t.z * kW13RowBytes);
+          prefetch_l2(s13 + (size_t)t.y * kHBlocks, t.z * kHBlocks);
+          prefetch_l2(s13 + (size_t)(kI + t.y) * kHBlocks, t.z * kHBlocks);
+        }
+      }
+    }
+    for (int u = warp; u < un; u += kWarps) {
+      const int4 t = tb.gu_tile[(u0 + u) / ks];
+      const int kp = (u0 + u) % ks;
+      const int slot = t.x, e = tb.slot_expert[slot];
+      const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
+      const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
+      const int pb = tb.slot_begin[slot], m = tb.slot_begin[slot + 1] - pb;
+      const uint8_t* xtok = (t.w + g < m) ? smem + (size_t)tb.pair_token[pb + t.w + g] * kXhBytes : nullptr;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint8_t* ring = const_cast<uint8_t*>(smem) + smem_layout(p.M).ring + (size_t)warp * kWarpRing;
+      gate_up_tile(q13, s13, t.y, t.z, xtok, kp * kpart, (kp + 1) * kpart, acc, ring, lane);
+      red[u * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+    __syncthreads();
+    for (int u = warp; u < un; u += kWarps) {
+      if ((u0 + u) % ks != 0) continue;
+      const int4 t = tb.gu_tile[(u0 + u) / ks];
+      float4 r = red[u * 32 + lane];
+      for (int k = 1; k < ks; ++k) {
+        const float4 o = red[(u + k) * 32 + lane];
+        r.x += o.x; r.y += o.y; r.z += o.z; r.w += o.w;
+      }
+      const int slot = t.x, pb = tb.slot_begin[slot], m = tb.slot_begin[slot + 1] - pb;
+      if (g < t.z) {
+        const float gv[2] = {r.x, r.y}, uv[2] = {r.z, r.w};
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = t.w + 2 * q + c;
+          if (col < m) {
+            const float sx = tb.sx[tb.pair_token[pb + col]];
+            const float gs = gv[c] * sx, us = uv[c] * sx;
+            p.h[(size_t)(pb + col) * kI + t.y + g] = gs / (1.0f + expf(-gs)) * us;
+          }
+        }
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -496,75 +656,166 @@ __device__ void quantise_pairs(const MoeParams& p, uint8_t* smem, Tables& tb, in
     uint8_t* hh = smem + smem_layout(p.M).hh + (size_t)k * kHhBytes;
 #pragma unroll
     for (int i = 0; i < kI / 32; ++i) {
-      const int e = lane + 32 * i, b = e >> 5, c = (e & 31) >> 3, o = e & 7;
+      const int e = lane + 32 * i;
       const uint32_t code = f32x2_to_e4m3x2(__fdiv_rn(v[i], s), 0.f) & 0xFF;
       const uint32_t f = e4m3x2_to_f16x2(code);
-      *reinterpret_cast<uint16_t*>(hh + (size_t)(c * kIBlocks + b) * 16 + o * 2) = (uint16_t)f;
+      *reinterpret_cast<uint16_t*>(hh + (size_t)e * 2) = (uint16_t)f;
       if (blockIdx.x == 0) p.hq[(size_t)q * kI + e] = (uint8_t)code;
     }
     if (blockIdx.x == 0 && lane == 0) p.sh[q] = s;
   }
 }
 
-constexpr int kDownBatch = 8;   // (row, pair) items whose loads a warp keeps in flight
-
+// Down projection + combine for the block's output rows [r0, r0 + nrows), in chunks of
+// kPairChunk pairs (their h quantised into shared memory first).
+//  * Full 16-row tiles on the tensor cores: m16n8k16 with A = 16 W2 rows (E2M1 -> f16),
+//    B = h-hat of up to 8 of the slot's tokens (f16), K = 768 split in two halves of 12
+//    blocks (one unit each, staged through the warp's cp.async ring); each block's fresh
+//    result is scaled by the row's E8M0 scale in fp32; the halves are added in a fixed order.
+//  * Leftover rows (nrows mod 16) on the CUDA cores, one warp per (slot, row).
+// Every (pair, row) result is multiplied by the pair's gate and h scale into `part`, and the
+// per-token sums are taken in pair order, so the output does not depend on scheduling.
 __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* smem, Tables& tb,
                              int layer) {
   const int M = p.M, G = gridDim.x;
   const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
-  const int nrows = r1 - r0;
+  const int nrows = r1 - r0, nfull = nrows / 16, nrem = nrows - 16 * nfull;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, qd = lane & 3;
   const Smem sl = smem_layout(M);
   float* part = reinterpret_cast<float*>(smem + sl.part);
   float* yacc = reinterpret_cast<float*>(smem + sl.yacc);
+  float4* red = reinterpret_cast<float4*>(smem + sl.gured);
+  uint8_t* ring = smem + sl.ring + (size_t)warp * kWarpRing;
   for (int i = threadIdx.x; i < M * kMaxRowsPerBlock; i += blockDim.x) yacc[i] = 0.f;
+  auto w2_of = [&](int slot, const uint8_t*& q2, const uint8_t*& s2) {
+    const int e = tb.slot_expert[slot];
+    q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
+    s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
+  };
   const int NP = tb.n_pairs;
   for (int q0 = 0; q0 < NP; q0 += kPairChunk) {
     const int n = min(kPairChunk, NP - q0);
     __syncthreads();
     quantise_pairs(p, smem, tb, q0, n);
-    __syncthreads();
-    // items (row, pair) of this chunk; a warp takes kDownBatch consecutive items, issues
-    // all their loads, then reduces each: lanes 0..23 hold one MX block of the row each
-    const int items = nrows * n;
-    for (int base = warp * kDownBatch; base < items; base += kWarps * kDownBatch) {
-      uint4 w[kDownBatch];
-      uint32_t sc[kDownBatch];
-#pragma unroll
-      for (int u = 0; u < kDownBatch; ++u) {
-        const int it = base + u;
-        w[u] = make_uint4(0, 0, 0, 0);
-        sc[u] = 0;
-        if (it < items && lane < kIBlocks) {
-          const int k = it % n, r = r0 + it / n;
-          const int e = tb.slot_expert[tb.pair_slot[q0 + k]];
-          const uint8_t* q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
-          const uint8_t* s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
-          w[u] = ldg_stream16(q2 + (size_t)r * kW2RowBytes + lane * 16);
-          sc[u] = ldg_stream_u8(s2 + (size_t)r * kIBlocks + lane);
-        }
+    // unit list: (slot, full tile, K half, 8-token group)
+    if (threadIdx.x == 0) {
+      int cnt = 0;
+      const int s_lo = tb.pair_slot[q0], s_hi = tb.pair_slot[q0 + n - 1];
+      for (int sidx = s_lo; sidx <= s_hi; ++sidx) {
+        const int pa = max(tb.slot_begin[sidx], q0), pz = min(tb.slot_begin[sidx + 1], q0 + n);
+        for (int tile = 0; tile < nfull; ++tile)
+          for (int ng = pa; ng < pz; ng += 8)
+            for (int kp = 0; kp < 2 && cnt < kGuMaxTiles; ++kp) tb.gu_tile[cnt++] = make_int4(sidx, tile, kp, ng);
       }
-#pragma unroll
-      for (int u = 0; u < kDownBatch; ++u) {
-        const int it = base + u;
-        if (it >= items) break;
-        const int k = it % n, rr = it / n;
-        float d = 0.f;
-        if (lane < kIBlocks) {
-          const uint8_t* hh = smem + sl.hh + (size_t)k * kHhBytes;
-          uint32_t x2[16];
-#pragma unroll
-          for (int pl = 0; pl < 4; ++pl) {
-            uint4 v = *reinterpret_cast<const uint4*>(hh + (size_t)(pl * kIBlocks + lane) * 16);
-            x2[4 * pl] = v.x; x2[4 * pl + 1] = v.y; x2[4 * pl + 2] = v.z; x2[4 * pl + 3] = v.w;
-          }
-          d = mx_block_dot(w[u], x2) * e8m0_to_f32(sc[u]);
-        }
-        d = warp_sum(d);
-        if (lane == 0) part[k * kMaxRowsPerBlock + rr] = d * tb.sh[k] * tb.pair_gate[q0 + k];
-      }
+      tb.gu_n = cnt;
     }
     __syncthreads();
+    MDW_TRACE_POINT(layer, 13);
+    const int units = tb.gu_n;
+    for (int u0 = 0; u0 < units; u0 += kGuRound) {
+      const int un = min(kGuRound, units - u0);
+      const int mine = un > warp ? (un - warp + kWarps - 1) / kWarps : 0;
+      auto issue = [&](int k) {
+        const int4 t = tb.gu_tile[u0 + warp + k * kWarps];
+        const uint8_t *q2, *s2;
+        w2_of(t.x, q2, s2);
+        uint8_t* dst = ring + (k % kDnStages) * kDnStageBytes;
+        const int rb = r0 + 16 * t.y, kb0 = t.z * kDnKB;
+#pragma unroll
+        for (int j = 0; j < 16 * kDnKB / 32; ++j) {     // 16 rows x 12 chunks of 16 bytes
+          const int c = lane + 32 * j, row = c / kDnKB, blk = c % kDnKB;
+          cp_async16(dst + row * kDnPitch + blk * 16, q2 + (size_t)(rb + row) * kW2RowBytes + (kb0 + blk) * 16);
+        }
+        if (lane < 16 * 3 / 2) {                         // 16 rows x 24 scale bytes, 8 at a time
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int c = lane + 24 * j, row = c / 3, part8 = c % 3;
+            cp_async8(dst + 16 * kDnPitch + row * kIBlocks + part8 * 8,
+                      s2 + (size_t)(rb + row) * kIBlocks + part8 * 8);
+          }
+        }
+      };
+      if (mine > 0) issue(0);
+      cp_async_commit();
+      for (int k = 0; k < mine; ++k) {
+        if (k + 1 < mine) issue(k + 1);
+        cp_async_commit();
+        cp_async_wait<kDnStages - 1>();
+        __syncwarp();
+        const uint8_t* buf = ring + (k % kDnStages) * kDnStageBytes;
+        const int4 t = tb.gu_tile[u0 + warp + k * kWarps];
+        const int pz = min(tb.slot_begin[t.x + 1], q0 + n);
+        const int kb0 = t.z * kDnKB;
+        // B column g = token pair t.w + g of the slot (if it exists in this chunk)
+        const uint8_t* hb = (t.w + g < pz) ? smem + sl.hh + (size_t)(t.w + g - q0) * kHhBytes : nullptr;
+        const uint8_t* sc_g = buf + 16 * kDnPitch + g * kIBlocks + kb0;
+        const uint8_t* sc_g8 = buf + 16 * kDnPitch + (g + 8) * kIBlocks + kb0;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int b = 0; b < kDnKB; ++b) {
+          const uint32_t wa = *reinterpret_cast<const uint32_t*>(buf + g * kDnPitch + b * 16 + 4 * qd);
+          const uint32_t wb = *reinterpret_cast<const uint32_t*>(buf + (g + 8) * kDnPitch + b * 16 + 4 * qd);
+          uint4 xv = make_uint4(0, 0, 0, 0);
+          if (hb) xv = *reinterpret_cast<const uint4*>(hb + 64 * (kb0 + b) + 16 * qd);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_16816(d, e2m1x2_to_f16x2(wa & 0xFF), e2m1x2_to_f16x2(wb & 0xFF),
+                    e2m1x2_to_f16x2((wa >> 8) & 0xFF), e2m1x2_to_f16x2((wb >> 8) & 0xFF), xv.x, xv.y);
+          mma_16816(d, e2m1x2_to_f16x2((wa >> 16) & 0xFF), e2m1x2_to_f16x2((wb >> 16) & 0xFF),
+                    e2m1x2_to_f16x2(wa >> 24), e2m1x2_to_f16x2(wb >> 24), xv.z, xv.w);
+          const float fa = e8m0_to_f32(sc_g[b]), fb = e8m0_to_f32(sc_g8[b]);
+          acc[0] = fmaf(fa, d[0], acc[0]);
+          acc[1] = fmaf(fa, d[1], acc[1]);
+          acc[2] = fmaf(fb, d[2], acc[2]);
+          acc[3] = fmaf(fb, d[3], acc[3]);
+        }
+        __syncwarp();
+        red[(warp + k * kWarps) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      }
+      __syncthreads();
+      // K halves added in order (unit kp = 0 owns the pair); D rows = W2 rows g, g + 8;
+      // D columns 2qd, 2qd + 1 = pairs t.w + 2qd (+1)
+      for (int u = warp; u < un; u += kWarps) {
+        const int4 t = tb.gu_tile[u0 + u];
+        if (t.z != 0) continue;
+        const float4 a0 = red[u * 32 + lane], a1 = red[(u + 1) * 32 + lane];
+        const float v[4] = {a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w};
+        const int pz = min(tb.slot_begin[t.x + 1], q0 + n);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int q = t.w + 2 * qd + c;
+          if (q >= pz) continue;
+          const int k2 = q - q0;
+          const float f = tb.sh[k2] * tb.pair_gate[q];
+          part[k2 * kMaxRowsPerBlock + 16 * t.y + g] = v[c] * f;
+          part[k2 * kMaxRowsPerBlock + 16 * t.y + g + 8] = v[2 + c] * f;
+        }
+      }
+    }
+    // leftover rows: one warp per (pair, row); lanes 0..23 one block each
+    const int rem_items = n * nrem;
+    for (int it = warp; it < rem_items; it += kWarps) {
+      const int k2 = it / nrem, rr = 16 * nfull + it % nrem, q = q0 + k2;
+      const uint8_t *q2, *s2;
+      w2_of(tb.pair_slot[q], q2, s2);
+      float dsum = 0.f;
+      if (lane < kIBlocks) {
+        const uint4 w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
+        const float sc = e8m0_to_f32(ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane));
+        const uint8_t* hh = smem + sl.hh + (size_t)k2 * kHhBytes + 64 * lane;
+        uint32_t x2[16];
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(hh + 16 * pl);
+          x2[4 * pl] = xv.x; x2[4 * pl + 1] = xv.y; x2[4 * pl + 2] = xv.z; x2[4 * pl + 3] = xv.w;
+        }
+        dsum = mx_block_dot(w, x2) * sc;
+      }
+      dsum = warp_sum(dsum);
+      if (lane == 0) part[k2 * kMaxRowsPerBlock + rr] = dsum * tb.sh[k2] * tb.pair_gate[q];
+    }
+    __syncthreads();
+    MDW_TRACE_POINT(layer, 14);
     // fixed-order accumulation over the chunk's pairs (ascending)
     for (int i = threadIdx.x; i < M * nrows; i += blockDim.x) {
       const int t = i / nrows, rr = i % nrows;
@@ -592,55 +843,44 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
   }
 }
 
-// ------------------------------------------------------------------ prefetch helpers
-
-__device__ void prefetch_static(const MoeParams& p, const LayerDesc& L) {
-  // this block's router rows and shared-expert slice of a layer (issued by one thread)
-  if (threadIdx.x != 0) return;
-  const int G = gridDim.x, E = p.E;
-  const int e0 = (int)((long long)blockIdx.x * E / G), e1 = (int)((long long)(blockIdx.x + 1) * E / G);
-  prefetch_l2(L.router_w + (size_t)e0 * kH, (uint32_t)((e1 - e0) * kH * 2));
-  if (p.has_shared) {
-    const int j0 = (int)((long long)blockIdx.x * kI / G), j1 = (int)((long long)(blockIdx.x + 1) * kI / G);
-    for (int half = 0; half < 2; ++half) {
-      const size_t row = (size_t)half * kI + j0;
-      prefetch_l2(L.sh_w13_q + row * kW13RowBytes, (uint32_t)((j1 - j0) * kW13RowBytes));
-      prefetch_l2(L.sh_w13_s + row * kHBlocks, (uint32_t)(((j1 - j0) * kHBlocks + 15) & ~15));
-    }
-  }
+// L2 prefetch of [base, base + bytes), one 128-byte line per thread per step, spread over
+// all threads of the block (non-blocking: the instructions carry no destination register).
+__device__ __forceinline__ void prefetch_range(const void* base, size_t bytes) {
+  const char* b = static_cast<const char*>(base);
+  for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)blockDim.x * 128)
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(b + off));
+  if (threadIdx.x == 0 && bytes > 0) asm volatile("prefetch.global.L2 [%0];" :: "l"(b + bytes - 1));
 }
 
-// L2 prefetch of the w13 rows (and scales) of virtual row pairs [a, b).
-__device__ void prefetch_gate_up(const LayerDesc& L, const Tables& tb, int a, int b, int slot_offset) {
-  if (threadIdx.x != 0) return;
-  while (a < b) {
-    const int slot = a / kI + slot_offset, j0 = a % kI;
-    const int j1 = min(kI, j0 + (b - a));
-    const int e = tb.slot_expert[slot];
-    const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
-    const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
-    for (int half = 0; half < 2; ++half) {
-      const size_t row = (size_t)half * kI + j0;
-      prefetch_l2(q13 + row * kW13RowBytes, (uint32_t)((j1 - j0) * kW13RowBytes));
-      const size_t sb = (row * kHBlocks) & ~(size_t)15;
-      const size_t se = (((row + (j1 - j0)) * kHBlocks) + 15) & ~(size_t)15;
-      prefetch_l2(s13 + sb, (uint32_t)(se - sb));
-    }
-    a += j1 - j0;
-  }
-}
-
+// The block's W2 rows (and scales) of every slot: lane 0 of warp (slot mod warps) issues
+// the two bulk L2 prefetches of a slot (rows r0..r1 of W2 are contiguous).
 __device__ void prefetch_down(const MoeParams& p, const LayerDesc& L, const Tables& tb) {
   const int G = gridDim.x;
   const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
-  for (int s = threadIdx.x; s < tb.n_slots; s += blockDim.x) {
+  if ((threadIdx.x & 31) != 0) return;
+  for (int s = threadIdx.x >> 5; s < tb.n_slots; s += kWarps) {
     const int e = tb.slot_expert[s];
     const uint8_t* q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
     const uint8_t* s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
     prefetch_l2(q2 + (size_t)r0 * kW2RowBytes, (uint32_t)((r1 - r0) * kW2RowBytes));
-    const size_t sb = (size_t)r0 * kIBlocks & ~(size_t)15;
+    const size_t sb = ((size_t)r0 * kIBlocks) & ~(size_t)15;
     const size_t se = ((size_t)r1 * kIBlocks + 15) & ~(size_t)15;
     prefetch_l2(s2 + sb, (uint32_t)(se - sb));
+  }
+}
+
+// This block's router rows and shared-expert slice of a layer (routing-independent).
+__device__ void prefetch_static(const MoeParams& p, const LayerDesc& L) {
+  const int G = gridDim.x, E = p.E;
+  const int e0 = (int)((long long)blockIdx.x * E / G), e1 = (int)((long long)(blockIdx.x + 1) * E / G);
+  prefetch_range(L.router_w + (size_t)e0 * kH, (size_t)(e1 - e0) * kH * 2);
+  if (p.has_shared) {
+    const int j0 = (int)((long long)blockIdx.x * kI / G), j1 = (int)((long long)(blockIdx.x + 1) * kI / G);
+    for (int half = 0; half < 2; ++half) {
+      const size_t row = (size_t)half * kI + j0;
+      prefetch_range(L.sh_w13_q + row * kW13RowBytes, (size_t)(j1 - j0) * kW13RowBytes);
+      prefetch_range(L.sh_w13_s + row * kHBlocks, (size_t)(j1 - j0) * kHBlocks);
+    }
   }
 }
 
@@ -654,36 +894,48 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
   const int G = gridDim.x;
   for (int layer = 0; layer < p.L; ++layer) {
     const LayerDesc& L = p.layers[layer];
+    MDW_TRACE_POINT(layer, 0);
     prepare_input<MAXM>(p, layer, smem, tb);
+    MDW_TRACE_POINT(layer, 1);
     router_rows(p, L, smem);
     bar.arrive();                                                   // B1 (logits)
+    MDW_TRACE_POINT(layer, 2);
     if (p.has_shared) {
       // shared expert: static slice of its row pairs, needs only x-hat
       if (threadIdx.x == 0) { tb.slot_expert[0] = -1; tb.slot_begin[0] = 0; tb.slot_begin[1] = p.M; }
       if (threadIdx.x < p.M) tb.pair_token[threadIdx.x] = threadIdx.x;
       __syncthreads();
       const int j0 = (int)((long long)blockIdx.x * kI / G), j1 = (int)((long long)(blockIdx.x + 1) * kI / G);
-      gate_up_range<MAXM>(p, L, smem, tb, j0, j1, 0);
+      build_gate_up_tiles(tb, j0, j1, 0, tb);
+      gate_up_tiles(p, L, smem, tb, false);
     }
+    MDW_TRACE_POINT(layer, 3);
     if (!bar.wait()) return;
-    route_tokens(p, tb, layer);
+    MDW_TRACE_POINT(layer, 4);
+    route_tokens(p, tb, layer, smem + smem_layout(p.M).gured);
     __syncthreads();
     if (tb.bad) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
     {
       const int first = p.has_shared ? 1 : 0;
       const long long PR = (long long)tb.n_routed * kI;
       const int a = (int)((long long)blockIdx.x * PR / G), b = (int)((long long)(blockIdx.x + 1) * PR / G);
-      prefetch_gate_up(L, tb, a, b, first);
+      MDW_TRACE_POINT(layer, 12);
       prefetch_down(p, L, tb);
-      gate_up_range<MAXM>(p, L, smem, tb, a, b, first);
+      MDW_TRACE_POINT(layer, 5);
+      build_gate_up_tiles(tb, a, b, first, tb);
+      gate_up_tiles(p, L, smem, tb, true);
     }
     bar.arrive();                                                   // B2 (h)
+    MDW_TRACE_POINT(layer, 6);
     if (p.stack_mode && layer + 1 < p.L) prefetch_static(p, p.layers[layer + 1]);
     if (!bar.wait()) return;
+    MDW_TRACE_POINT(layer, 7);
     down_combine(p, L, smem, tb, layer);
+    MDW_TRACE_POINT(layer, 8);
     if (p.stack_mode && layer + 1 < p.L) {
       if (!bar.sync()) return;                                      // B3 (r_{l+1})
     }
+    MDW_TRACE_POINT(layer, 9);
   }
 }
 
@@ -700,6 +952,12 @@ cudaError_t launch_t(const MoeParams& p, cudaStream_t s) {
 }  // namespace
 
 size_t moe_smem_bytes(int M) { return smem_layout(M).total; }
+
+#ifdef MDW_TRACE
+extern "C" int mdw_trace_read(void* dst, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(dst, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+#endif
 
 cudaError_t launch_moe(const MoeParams& p, cudaStream_t s) {
   if (p.M <= 1) return launch_t<1>(p, s);
