@@ -18,7 +18,7 @@ int device_sm_count() {
   return n;
 }
 int moe_grid() { return device_sm_count(); }
-int head_grid() { const int n = device_sm_count(); return n > 256 ? 256 : n; }
+int head_grid() { const int n = device_sm_count(); return n > kMaxHeadGrid ? kMaxHeadGrid : n; }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -129,7 +129,7 @@ mdw_status head_call(const mdw_lm_head* head, int fmt, int32_t M, const void* h_
   hp.topk_idx = topk_idx;
   hp.topk_val = topk_val;
   hp.hdr = hdr;
-  const size_t n = (size_t)head_grid() * M * topk;
+  const size_t n = (size_t)(head_grid() + kHeadMaxGroups) * M * topk;
   hp.cand_val = reinterpret_cast<float*>(cand);
   hp.cand_idx = reinterpret_cast<int32_t*>(cand + align_up(n * 4, 256));
   return cuda_status(fmt == MDW_FMT_FP8_E4M3_ROWSCALE ? launch_head_fp8(hp, s) : launch_head_bf16(hp, s));
@@ -256,7 +256,8 @@ size_t mdw_lm_head_workspace_bytes(const mdw_lm_head* head, int32_t M, int32_t t
   if (!head || M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK) return 0;
   const int g = head_grid();
   if (g <= 0) return 0;
-  return kHdrWords * 4 + align_up((size_t)g * M * topk * 4, 256) + align_up((size_t)g * M * topk * 4, 256);
+  const size_t n = (size_t)(g + kHeadMaxGroups) * M * topk;     // block lists + group lists
+  return kHdrWords * 4 + align_up(n * 4, 256) + align_up(n * 4, 256);
 }
 
 mdw_status lm_head_fp8(const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,

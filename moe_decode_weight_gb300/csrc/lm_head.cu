@@ -9,10 +9,11 @@
 // among the top_k = 29 tokens, and the synthetic run is greedy (arg-max).
 //
 // GB300 mapping: one block of 384 threads per SM, each block a contiguous slice of
-// ~V/152 vocabulary rows; one warp per row at a time (a 2,560-byte FP8 row is exactly five
-// 16-byte loads per lane), per-row scale applied after the warp reduction; each warp keeps
-// its running top-k per token in registers (lane i holds the i-th best), the block merges
-// its warps' lists, and the last block to finish merges all blocks' lists.
+// ~V/152 vocabulary rows, each warp walking 16-row tiles of the slice on m16n8k16 tensor-core
+// MMAs (rows x tokens, fp32 accumulation; FP8 weights converted exactly to f16 in
+// registers), the per-row scale applied once per logit; each warp keeps its running top-k
+// per token in registers (lane i holds the i-th best), the block merges its warps' lists,
+// and the last block to finish merges all blocks' lists.
 #include "mdw_device.cuh"
 #include "mdw_internal.h"
 
@@ -20,16 +21,48 @@ namespace mdw {
 namespace {
 
 constexpr int kHeadThreads = kThreads;
-constexpr int kMaxTK = 32;               // candidates per token per warp (lane-distributed)
-constexpr int kMergeCap = 256;           // compacted candidates per warp during a merge
-constexpr int kMaxHeadGrid = 256;        // blocks of the head kernel (one per SM)
+constexpr int kMaxTK = 32;               // list length (lane-distributed; tk <= 32)
+// Built only with -DMDW_TRACE (a profiling build, never the product build): %globaltimer at
+// the head kernel's phase boundaries, per block ([0] start, [1] hidden states ready, [2] all
+// tiles done, [3] block list written, [4] group merge starts, [5] final merge starts, [6]
+// end) and per warp ([8 + warp] its last unit done).
+#ifdef MDW_TRACE
+__device__ unsigned long long g_head_trace[kMaxHeadGrid * 24];
+__device__ __forceinline__ void head_trace(int slot) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  g_head_trace[blockIdx.x * 24 + slot] = t;
+}
+#define MDW_HEAD_TRACE(cond, slot) do { if (cond) head_trace(slot); } while (0)
+#else
+#define MDW_HEAD_TRACE(cond, slot) do { } while (0)
+#endif
+#ifndef MDW_HEAD_U
+#define MDW_HEAD_U 4                     // 64-byte chunks per row whose loads a warp keeps in flight
+#endif
+#ifndef MDW_HEAD_PF
+#define MDW_HEAD_PF 4                    // units a warp prefetches into L2 ahead of its loads
+#endif
 
-__host__ __device__ inline size_t head_smem_bytes(int M, int MAXM) {
-  // xs [M][H] fp32 (its bytes later hold the warp lists [MAXM][warps][32] x 2 and the global
-  // merge's [M][kMergeCap] x 2), thresholds / counters [MAXM] x 3, results [MAXM][32] x 2,
-  // per-warp merge scratch [warps][kMergeCap] x 2
-  return (size_t)M * kH * 4 + (size_t)MAXM * 12 + (size_t)MAXM * kMaxTK * 8 +
-         (size_t)kWarps * kMergeCap * 8 + 64;
+// Bytes per token row of the hidden states in shared memory (padded so the MMA B-fragment
+// reads of different tokens fall in different banks).
+template <bool FP8>
+__host__ __device__ constexpr int head_x_stride() { return FP8 ? 2 * kH + 16 : 2 * kH + 64; }
+
+// Region 0 holds the hidden states [M][xstride] during the tiles; afterwards the lists
+// [MAXM][warps][32] (values, then indices) followed by the split tiles' partial sums
+// [warps][2][NT][32 lanes][4].
+__host__ __device__ inline size_t head_lists_bytes(int MAXM) { return (size_t)MAXM * kWarps * kMaxTK * 8; }
+__host__ __device__ inline size_t head_region0_bytes(int M, int MAXM, int xstride) {
+  const int NT = (MAXM + 7) / 8;
+  size_t r = (size_t)M * xstride;
+  const size_t after = head_lists_bytes(MAXM) + (size_t)kWarps * 2 * NT * 32 * 16;
+  if (after > r) r = after;
+  return (r + 15) & ~(size_t)15;
+}
+// + per-token x multipliers, 1/rms, scale exponents and partial reductions [MAXM][10]
+__host__ __device__ inline size_t head_smem_bytes(int M, int MAXM, int xstride) {
+  return head_region0_bytes(M, MAXM, xstride) + (size_t)MAXM * 13 * 4 + 64;
 }
 
 // ------------------------------------------------------------------ quantisation
@@ -71,18 +104,21 @@ __global__ void __launch_bounds__(256) quantize_head_kernel(const __nv_bfloat16*
 
 // ------------------------------------------------------------------ top-k lists
 
-// Lane-distributed sorted list (lane i = i-th best; lanes >= tk hold -inf).
+// Lane-distributed sorted list (lane i = i-th best under `beats`; unused lanes hold the
+// pad (-inf, INT_MAX), which every real candidate beats).
 struct WarpList {
   float v;
   int i;
-  float thr_v;   // warp-uniform copy of entry tk-1
+  float thr_v;   // warp-uniform copy of entry tk-1 (the bar a new candidate must beat)
   int thr_i;
 };
+constexpr int kPadIdx = 0x7fffffff;
 
 __device__ __forceinline__ void list_init(WarpList& L) {
-  L.v = -INFINITY; L.i = 0x7fffffff; L.thr_v = -INFINITY; L.thr_i = 0x7fffffff;
+  L.v = -INFINITY; L.i = kPadIdx; L.thr_v = -INFINITY; L.thr_i = kPadIdx;
 }
 
+// Insert one warp-uniform candidate (no-op unless it beats entry tk-1).
 __device__ __forceinline__ void list_insert(WarpList& L, float v, int idx, int tk, int lane) {
   if (!beats(v, idx, L.thr_v, L.thr_i)) return;           // warp-uniform decision
   const unsigned better = __ballot_sync(0xffffffffu, lane < tk && beats(L.v, L.i, v, idx));
@@ -97,349 +133,490 @@ __device__ __forceinline__ void list_insert(WarpList& L, float v, int idx, int t
   L.thr_i = __shfl_sync(0xffffffffu, L.i, tk - 1);
 }
 
-// Top-tk (descending) of n candidates by one warp. Only candidates not worse than the
-// threshold (tv, ti) can qualify: they are first compacted into tmp (capacity cap), then
-// tk rounds of warp arg-max pick them in order. load(k) returns candidate k. If more than
-// cap candidates pass, the rounds scan the candidates directly (slower, same result).
-template <typename Load>
-__device__ void warp_topk(Load load, int n, int tk, float tv, int ti, float* tmpv, int* tmpi, int cap,
-                          float* outv, int* outi, int lane) {
-  int count = 0;
-  for (int k0 = 0; k0 < n; k0 += 32) {
-    const int k = k0 + lane;
-    float v = -INFINITY;
-    int i = 0x7fffffff;
-    bool keep = false;
-    if (k < n) { load(k, v, i); keep = !beats(tv, ti, v, i); }
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    const int pos = count + __popc(m & ((1u << lane) - 1u));
-    if (keep && pos < cap) { tmpv[pos] = v; tmpi[pos] = i; }
-    count += __popc(m);
+// (v, i) <- the 32 best of the union of two descending lane-distributed lists (v, i) and
+// (bv, bi): pairing entry j of one with entry 31 - j of the other and keeping the better
+// gives a bitonic sequence holding the 32 best; a descending bitonic merge (five
+// compare-exchange stages) sorts it. The first tk lanes are then the top-tk of the union
+// whenever each input holds its own top-tk.
+__device__ __forceinline__ void list_merge(float& v, int& i, float bv, int bi, int lane) {
+  const float rv = __shfl_sync(0xffffffffu, bv, 31 - lane);
+  const int ri = __shfl_sync(0xffffffffu, bi, 31 - lane);
+  if (beats(rv, ri, v, i)) { v = rv; i = ri; }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (((lane & o) == 0) == beats(ov, oi, v, i)) { v = ov; i = oi; }
   }
-  __syncwarp();
-  const bool compact = count <= cap;
-  float pv = INFINITY;
-  int pi = -1;
-  for (int r = 0; r < tk; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    const int lim = compact ? count : n;
-    for (int k = lane; k < lim; k += 32) {
-      float v;
-      int i;
-      if (compact) { v = tmpv[k]; i = tmpi[k]; } else { load(k, v, i); }
-      if (beats(tv, ti, v, i) || !beats(pv, pi, v, i)) continue;   // below threshold / taken
-      if (beats(v, i, bv, bi)) { bv = v; bi = i; }
+}
+
+// Block-wide tree merge of the lists S[t][w] (w < warps, 32 entries each, values at sv and
+// indices at si, index (t * warps + w) * 32 + lane) into S[t][0], for every token t < M.
+// Level s merges list w + s into list w for w a multiple of 2s; the (token, pair) merges
+// of a level are spread over the warps. Every thread of the block must call it.
+__device__ void tree_merge(float* sv, int* si, int M, int warp, int lane) {
+  __syncthreads();
+#pragma unroll 1
+  for (int s = 1; s < kWarps; s <<= 1) {
+    int np = 0;
+    for (int w = 0; w + s < kWarps; w += 2 * s) ++np;
+    for (int job = warp; job < M * np; job += kWarps) {
+      const int t = job / np, w = (job % np) * 2 * s;
+      const int a = (t * kWarps + w) * kMaxTK + lane, b = (t * kWarps + w + s) * kMaxTK + lane;
+      float v = sv[a];
+      int i = si[a];
+      list_merge(v, i, sv[b], si[b], lane);
+      sv[a] = v;
+      si[a] = i;
     }
-    warp_argmax(bv, bi);
-    pv = bv; pi = bi;
-    if (lane == 0) { outv[r] = bv; outi[r] = bi; }
+    __syncthreads();
   }
-  __syncwarp();
+}
+
+// Loads the lists j < n of every token (list j of token t at cv / ci + ((first + j) * M + t)
+// * tk, tk entries, written by other blocks of this launch), merges them into S[t][0].
+// Warp w takes lists w, w + warps, ... of each token (n <= 2 * warps).
+template <int MAXM>
+__device__ void merge_global_lists(const float* cv, const int* ci, int first, int n, int M, int tk,
+                                   float* sv, int* si, int warp, int lane) {
+  float av[MAXM], bv[MAXM];
+  int ai[MAXM], bi[MAXM];
+#pragma unroll
+  for (int t = 0; t < MAXM; ++t) {             // issue every load before the first merge
+    av[t] = bv[t] = -INFINITY;
+    ai[t] = bi[t] = kPadIdx;
+    if (t < M && lane < tk) {
+      if (warp < n) {
+        const size_t o = ((size_t)(first + warp) * M + t) * tk + lane;
+        av[t] = ld_cg_f32(cv + o);
+        ai[t] = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(ci) + o));
+      }
+      if (warp + kWarps < n) {
+        const size_t o = ((size_t)(first + warp + kWarps) * M + t) * tk + lane;
+        bv[t] = ld_cg_f32(cv + o);
+        bi[t] = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(ci) + o));
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < MAXM; ++t) {
+    if (t < M) {
+      if (warp + kWarps < n) list_merge(av[t], ai[t], bv[t], bi[t], lane);
+      sv[(t * kWarps + warp) * kMaxTK + lane] = av[t];
+      si[(t * kWarps + warp) * kMaxTK + lane] = ai[t];
+    }
+  }
+  tree_merge(sv, si, M, warp, lane);
 }
 
 // ------------------------------------------------------------------ GEMV
 
-template <bool FP8>
-struct RowLoad {
-  uint4 q[FP8 ? 5 : 10];
-};
-
-// Dot products of one row with the M tokens' hidden states (fp32 in shared memory, or in
-// registers when M == 1), returned warp-reduced in acc[t].
-template <bool FP8, int MAXM>
-__device__ __forceinline__ void row_dot(const RowLoad<FP8>& ld, const float* xs, const float (&xr)[80],
-                                        int M, int lane, float (&acc)[MAXM]) {
-#pragma unroll
-  for (int t = 0; t < MAXM; ++t) acc[t] = 0.f;
-  constexpr int NC = FP8 ? 5 : 10;
-  constexpr int EPC = FP8 ? 16 : 8;        // elements per 16-byte chunk
-#pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    float w[EPC];
-    const uint32_t a[4] = {ld.q[c].x, ld.q[c].y, ld.q[c].z, ld.q[c].w};
-    if (FP8) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t lo = e4m3x2_to_f16x2(a[k] & 0xFFFF), hi = e4m3x2_to_f16x2(a[k] >> 16);
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-        w[4 * k] = f0.x; w[4 * k + 1] = f0.y; w[4 * k + 2] = f1.x; w[4 * k + 3] = f1.y;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        w[2 * k] = __uint_as_float(a[k] << 16);
-        w[2 * k + 1] = __uint_as_float(a[k] & 0xFFFF0000u);
-      }
-    }
-    const int e0 = (32 * c + lane) * EPC;   // first hidden index of this chunk
-#pragma unroll
-    for (int t = 0; t < MAXM; ++t) {
-      if (t < M) {
-        float s0 = acc[t];
-        if (MAXM == 1) {
-#pragma unroll
-          for (int k = 0; k < EPC; ++k) s0 = fmaf(w[k], xr[c * EPC + k], s0);
-        } else {
-          const float4* x4 = reinterpret_cast<const float4*>(xs + (size_t)t * kH + e0);
-#pragma unroll
-          for (int k = 0; k < EPC / 4; ++k) {
-            const float4 xv = x4[k];
-            s0 = fmaf(w[4 * k], xv.x, s0);
-            s0 = fmaf(w[4 * k + 1], xv.y, s0);
-            s0 = fmaf(w[4 * k + 2], xv.z, s0);
-            s0 = fmaf(w[4 * k + 3], xv.w, s0);
-          }
-        }
-        acc[t] = s0;
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < MAXM; ++t)
-    if (t < M) acc[t] = warp_sum(acc[t]);
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// tk-th best (value, index) among the warp's register-held candidates (PER per lane),
-// by tk rounds of warp arg-max; every lane gets the result.
-template <int PER>
-__device__ void warp_kth(const float (&v)[PER], const int (&ix)[PER], int tk, float& kv, int& ki) {
-  float pv = INFINITY;
-  int pi = -1;
-  for (int r = 0; r < tk; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < PER; ++j)
-      if (beats(pv, pi, v[j], ix[j]) && beats(v[j], ix[j], bv, bi)) { bv = v[j]; bi = ix[j]; }
-    warp_argmax(bv, bi);
-    pv = bv; pi = bi;
-  }
-  kv = pv; ki = pi;
-}
-
+// The head GEMV on the tensor cores. The block's vocabulary slice is cut into 16-row
+// tiles, each tile's K into NG units of U 64-byte chunks, and the (tile, unit) sequence into
+// 12 equal contiguous ranges, one per warp (so every warp streams the same number of
+// bytes; a tile cut between warps is finished from the warps' partial sums afterwards).
+// Per tile: D[16 rows][8 tokens] = W[16 rows][K] x X^T on m16n8k16 MMAs with fp32
+// accumulation, then logit = D * row scale (FP8: E4M3 weights -> f16 exactly, hidden states
+// as f16 under a per-token power-of-two scale that keeps them inside the f16 range; BF16:
+// bf16 operands). Lane (g, q) loads bytes 16q..16q+15 of each chunk of rows g and g + 8
+// (full 32-byte sectors per warp load) and the matching hidden-state values, i.e. the
+// MMAs run on a permuted K order that is the same for W and X.
 template <bool FP8, int MAXM>
 __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  // xs [M][H] fp32 hidden states; after the row loop the same bytes hold the warps' lists
-  // (mv / mi) and, in the last block, the global merge's compacted candidates
-  float* xs = reinterpret_cast<float*>(smem);
-  float* mv = xs;                                                         // [M][warps][32]
-  int* mi = reinterpret_cast<int*>(mv + MAXM * kWarps * kMaxTK);
-  float* thv = reinterpret_cast<float*>(smem + (size_t)p.M * kH * 4);     // [M] per-token thresholds
-  int* thi = reinterpret_cast<int*>(thv + MAXM);
-  int* cnt = thi + MAXM;                                                  // [M] compaction counters
-  float* ov = reinterpret_cast<float*>(cnt + MAXM);                       // [M][32] results
-  int* oi = reinterpret_cast<int*>(ov + MAXM * kMaxTK);
-  float* tv_s = reinterpret_cast<float*>(oi + MAXM * kMaxTK);             // per-warp scratch (block merge)
-  int* ti_s = reinterpret_cast<int*>(tv_s + kWarps * kMergeCap);
-  __shared__ int is_last;
+  constexpr int XS = head_x_stride<FP8>();
+  constexpr int NT = (MAXM + 7) / 8;                 // 8-token column groups
   const int M = p.M, tk = p.topk;
+  uint8_t* xsm = smem;                                // [M][XS] hidden states (MMA operand)
+  float* lv = reinterpret_cast<float*>(smem);         // [MAXM][warps][32] list values
+  int* li = reinterpret_cast<int*>(smem + (size_t)MAXM * kWarps * kMaxTK * 4);
+  float* rec = reinterpret_cast<float*>(smem + head_lists_bytes(MAXM));   // split-tile partials
+  float* tokv = reinterpret_cast<float*>(smem + head_region0_bytes(M, MAXM, XS));
+  float* xmul = tokv;                                 // [MAXM] 2^k (FP8 f16 scaling)
+  float* tinv = tokv + MAXM;                          // [MAXM] 1 / rms
+  int* tkexp = reinterpret_cast<int*>(tokv + 2 * MAXM);   // [MAXM] k
+  float* part = tokv + 3 * MAXM;                      // [MAXM][10]
+  __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
   const long long G = gridDim.x;
   const long long v0 = blockIdx.x * p.V / G, v1 = (blockIdx.x + 1) * p.V / G;
   constexpr int ROWB = FP8 ? kH : 2 * kH;
-  constexpr int NC = FP8 ? 5 : 10;
-  constexpr int EPC = FP8 ? 16 : 8;
-  constexpr int kAhead = 4;                 // rows a warp prefetches into L2 ahead of use
+  constexpr int NCH = ROWB / 64;                      // 64-byte chunks per row
+  constexpr int U = MDW_HEAD_U;                       // chunks per unit (loads in flight together)
+  constexpr int NG = NCH / U;                         // units per tile
+  static_assert(U % 4 == 0 && NCH % U == 0, "units must tile a row in whole 128-byte lines");
+  const int ntile = (int)((v1 - v0 + 15) / 16);
+  const int total = ntile * NG;
+  auto ubeg = [&](int w) { return (int)((long long)w * total / kWarps); };
+  const int u0 = ubeg(warp), u1 = ubeg(warp + 1);
+  MDW_HEAD_TRACE(threadIdx.x == 0, 0);
 
-  // prefetch this warp's first rows while the hidden states are prepared
-  if (lane == 0)
-    for (int a = 0; a < kAhead; ++a) {
-      const long long v = v0 + warp + (long long)a * kWarps;
-      if (v < v1) prefetch_l2(p.w + v * ROWB, ROWB);
-    }
-
-  // hidden states -> fp32 shared memory (optionally bf16(RMSNorm(.)) first); all threads,
-  // 16-byte loads, fixed-order per-token reductions
-  {
-    float* part = tv_s;                      // [M][10] partial sums of squares
-    for (int c = threadIdx.x; c < M * (kH / 8); c += blockDim.x) {
-      const int t = c / (kH / 8), i = c % (kH / 8);
-      const uint4 u = ld_cg16(reinterpret_cast<const uint4*>(p.x + (size_t)t * kH) + i);
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-      float ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float a = __uint_as_float(w4[k] << 16), b = __uint_as_float(w4[k] & 0xFFFF0000u);
-        xs[(size_t)t * kH + 8 * i + 2 * k] = a;
-        xs[(size_t)t * kH + 8 * i + 2 * k + 1] = b;
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
+  // L2 prefetch of unit u of this warp: 16 rows x 64U bytes as whole 128-byte lines
+  auto prefetch_unit = [&](int u) {
+    if (u >= u1) return;
+    const int tl = u / NG, gi = u % NG;
+    constexpr int LPR = U / 2;                         // lines per row per unit
+    for (int pl = lane; pl < 16 * LPR; pl += 32) {
+      const long long row = v0 + 16LL * tl + pl / LPR;
+      if (row < v1) {
+        const uint8_t* a = p.w + row * ROWB + 64 * U * gi + 128 * (pl % LPR);
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(a));
       }
-      ss = warp_sum(ss);                    // a warp's 32 chunks belong to one token (320 % 32 == 0)
-      if (lane == 0) part[t * 10 + i / 32] = ss;
     }
-    __syncthreads();
+  };
+
+  // hidden states -> shared memory, every chunk loaded once into registers: bf16 values
+  // (optionally bf16(RMSNorm(.))), FP8 path then f16(x * 2^-k) with k = floor(log2 amax) - 14
+  {
+    constexpr int CPT = kH / 8;                       // 16-byte chunks per token
+    constexpr int CH = (MAXM * CPT + kHeadThreads - 1) / kHeadThreads;
+    uint32_t xr[CH][4];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int c = threadIdx.x + j * kHeadThreads;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (c < M * CPT) u = ld_cg16(reinterpret_cast<const uint4*>(p.x) + c);
+      xr[j][0] = u.x; xr[j][1] = u.y; xr[j][2] = u.z; xr[j][3] = u.w;
+    }
+    for (int n = 0; n < MDW_HEAD_PF; ++n) prefetch_unit(u0 + n);
+    // per-token reductions: a warp's 32 chunks belong to one token (320 % 32 == 0, 384 % 32 == 0)
+    auto reduce = [&](bool sq) {
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int c = threadIdx.x + j * kHeadThreads;
+        if (j * kHeadThreads + warp * 32 >= M * CPT) break;      // warp-uniform
+        float r = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = __uint_as_float(xr[j][k] << 16), b = __uint_as_float(xr[j][k] & 0xFFFF0000u);
+          if (sq) { r = fmaf(a, a, r); r = fmaf(b, b, r); }
+          else r = fmaxf(r, fmaxf(fabsf(a), fabsf(b)));
+        }
+        r = sq ? warp_sum(r) : warp_max(r);
+        if (lane == 0) part[(c / CPT) * 10 + (c % CPT) / 32] = r;
+      }
+      __syncthreads();
+    };
     if (p.norm_input) {
+      reduce(true);
       if (threadIdx.x < M) {
         float ss = 0.f;
         for (int j = 0; j < 10; ++j) ss += part[threadIdx.x * 10 + j];
-        thv[threadIdx.x] = rsqrtf(ss / (float)kH + 1e-6f);
+        tinv[threadIdx.x] = rsqrtf(ss / (float)kH + 1e-6f);
       }
       __syncthreads();
-      for (int e = threadIdx.x; e < M * kH; e += blockDim.x)
-        xs[e] = __bfloat162float(__float2bfloat16_rn(xs[e] * thv[e / kH]));
-      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int c = threadIdx.x + j * kHeadThreads;
+        if (c < M * CPT) {
+          const float inv = tinv[c / CPT];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 r2 = __floats2bfloat162_rn(__uint_as_float(xr[j][k] << 16) * inv,
+                                                            __uint_as_float(xr[j][k] & 0xFFFF0000u) * inv);
+            xr[j][k] = *reinterpret_cast<const uint32_t*>(&r2);
+          }
+        }
+      }
+      __syncthreads();                                 // part is reused below
     }
-  }
-  float xr[80];
-  if (MAXM == 1) {
+    if (FP8) {
+      reduce(false);
+      if (threadIdx.x < M) {
+        float am = 0.f;
+        for (int j = 0; j < 10; ++j) am = fmaxf(am, part[threadIdx.x * 10 + j]);
+        // scaled values lie below 2^15 (f16 max 65504) and the small ones stay clear of the
+        // f16 subnormal range; every step is a power of two, so only the f16 rounding of
+        // values far below amax is inexact
+        int e = 0;
+        frexpf(am, &e);                                // am = m * 2^e, m in [0.5, 1)
+        const int k = (am > 0.f && am < INFINITY) ? max(-100, min(100, e - 15)) : 0;
+        xmul[threadIdx.x] = ldexpf(1.0f, k);
+        tkexp[threadIdx.x] = k;
+      }
+      __syncthreads();
+    } else if (threadIdx.x < M) {
+      xmul[threadIdx.x] = 1.0f;
+    }
 #pragma unroll
-    for (int c = 0; c < NC; ++c)
+    for (int j = 0; j < CH; ++j) {
+      const int c = threadIdx.x + j * kHeadThreads;
+      if (c < M * CPT) {
+        const int t = c / CPT, i = c % CPT;
+        uint32_t o[4];
+        if (FP8) {
+          const int k = tkexp[t];
 #pragma unroll
-      for (int k = 0; k < EPC; ++k) xr[c * EPC + k] = xs[(32 * c + lane) * EPC + k];
+          for (int m2 = 0; m2 < 4; ++m2) {
+            const __half2 hh = __floats2half2_rn(ldexpf(__uint_as_float(xr[j][m2] << 16), -k),
+                                                 ldexpf(__uint_as_float(xr[j][m2] & 0xFFFF0000u), -k));
+            o[m2] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+        } else {
+#pragma unroll
+          for (int m2 = 0; m2 < 4; ++m2) o[m2] = xr[j][m2];
+        }
+        *reinterpret_cast<uint4*>(xsm + (size_t)t * XS + 16 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    __syncthreads();
   }
+  MDW_HEAD_TRACE(threadIdx.x == 0, 1);
 
   WarpList lst[MAXM];
 #pragma unroll
   for (int t = 0; t < MAXM; ++t) list_init(lst[t]);
+  constexpr int STEPS = FP8 ? 4 : 2;                  // k16 steps per 64-byte chunk
 
-  auto load_row = [&](long long v, RowLoad<FP8>& ld) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.w + v * ROWB);
+  // logits of a finished tile (sums d of rows vt + g (+8), tokens 8nt + 2q (+1)) -> lists
+  auto finish_tile = [&](int tl, float (&d)[NT][4]) {
+    const long long vt = v0 + 16LL * tl;
+    const bool va_ok = vt + g < v1, vb_ok = vt + g + 8 < v1;
+    const float sa = (FP8 && va_ok) ? p.row_scale[vt + g] : 1.0f;
+    const float sb = (FP8 && vb_ok) ? p.row_scale[vt + g + 8] : 1.0f;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) ld.q[c] = ldg_stream16(src + 32 * c + lane);
-  };
-  long long v = v0 + warp;
-  RowLoad<FP8> cur, nxt;
-  float sc_cur = 1.f, sc_nxt = 1.f;
-  if (v < v1) { load_row(v, cur); if (FP8) sc_cur = p.row_scale[v]; }
-  while (v < v1) {
-    const long long vn = v + kWarps;
-    if (lane == 0) {
-      const long long vp = v + (long long)kAhead * kWarps;
-      if (vp < v1) prefetch_l2(p.w + vp * ROWB, ROWB);
-    }
-    if (vn < v1) { load_row(vn, nxt); if (FP8) sc_nxt = p.row_scale[vn]; }
-    float acc[MAXM];
-    row_dot<FP8, MAXM>(cur, xs, xr, M, lane, acc);
+    for (int nt = 0; nt < NT; ++nt) {
+      float lg[4];
 #pragma unroll
-    for (int t = 0; t < MAXM; ++t) {
-      if (t < M) {
-        const float logit = acc[t] * sc_cur;
-        if (p.logits && lane == 0) p.logits[(size_t)t * p.V + v] = logit;
-        list_insert(lst[t], logit, (int)v, tk, lane);
+      for (int j = 0; j < 4; ++j) {
+        const int tok = 8 * nt + 2 * q + (j & 1);
+        const bool okr = (j < 2) ? va_ok : vb_ok;
+        lg[j] = d[nt][j] * ((j < 2) ? sa : sb) * (tok < M ? xmul[tok] : 1.0f);
+        if (p.logits && okr && tok < M) p.logits[(size_t)tok * p.V + vt + g + ((j >> 1) << 3)] = lg[j];
       }
-    }
-    cur = nxt;
-    sc_cur = sc_nxt;
-    v = vn;
-  }
-
-  // block merge: every warp writes its lists; warp t merges token t (threshold = best of
-  // the warps' tk-th entries, so at least tk entries survive)
-  __syncthreads();                          // xs is dead from here on: its bytes hold the lists
 #pragma unroll
-  for (int t = 0; t < MAXM; ++t) {
-    if (t < M) {
-      mv[(t * kWarps + warp) * kMaxTK + lane] = lst[t].v;
-      mi[(t * kWarps + warp) * kMaxTK + lane] = lst[t].i;
-    }
-  }
-  __syncthreads();
-  for (int t = warp; t < M; t += kWarps) {
-    float tv = -INFINITY;
-    int ti = 0x7fffffff;
-    if (lane < kWarps) {
-      tv = mv[(t * kWarps + lane) * kMaxTK + tk - 1];
-      ti = mi[(t * kWarps + lane) * kMaxTK + tk - 1];
-    }
-    warp_argmax(tv, ti);
-    const float* lv = mv + t * kWarps * kMaxTK;
-    const int* li = mi + t * kWarps * kMaxTK;
-    auto ld = [&](int k, float& vv, int& ii) { vv = lv[k]; ii = li[k]; };
-    float* outv = ov + t * kMaxTK;
-    int* outi = oi + t * kMaxTK;
-    warp_topk(ld, kWarps * kMaxTK, tk, tv, ti, tv_s + warp * kMergeCap, ti_s + warp * kMergeCap, kMergeCap,
-              outv, outi, lane);
-    const size_t o = ((size_t)blockIdx.x * M + t) * tk;
-    for (int r = lane; r < tk; r += 32) { p.cand_val[o + r] = outv[r]; p.cand_idx[o + r] = outi[r]; }
-  }
-
-  // the last block to finish merges all blocks' candidates
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.hdr + kHdrDoneCtr, 1u) == (uint32_t)(G - 1));
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  const int n = (int)(G * tk);
-  auto cand = [&](int t, int k, float& vv, int& ii) {
-    const size_t o = ((size_t)(k / tk) * M + t) * tk + (k % tk);
-    vv = ld_cg_f32(p.cand_val + o);
-    ii = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(p.cand_idx + o)));
-  };
-  // A. per token, the tk-th best of the blocks' first entries: tk distinct entries are not
-  //    worse than it, so it bounds the global tk-th entry from below
-  for (int t = warp; t < M; t += kWarps) {
-    constexpr int PER = kMaxHeadGrid / 32;
-    float fv[PER];
-    int fi[PER];
+      for (int t8 = 0; t8 < 8; ++t8) {
+        const int t = 8 * nt + t8;
+        if (t >= M) break;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {                       // one load per block, all in flight
-      const int b = lane + 32 * j;
-      fv[j] = -INFINITY;
-      fi[j] = 0x7fffffff;
-      if (b < G) cand(t, b * tk, fv[j], fi[j]);
-    }
-    float kv;
-    int ki;
-    warp_kth<PER>(fv, fi, tk, kv, ki);
-    if (lane == 0) { thv[t] = kv; thi[t] = ki; cnt[t] = 0; }
-  }
-  __syncthreads();
-  // B. all threads: compact the candidates not worse than their token's threshold
-  float* cv_s = xs;                                        // reuse (lists are dead): [M][kMergeCap]
-  int* ci_s = reinterpret_cast<int*>(xs + (size_t)M * kMergeCap);
-  constexpr int kScan = 8;                                 // loads in flight per thread
-  for (int e0 = 0; e0 < M * n; e0 += blockDim.x * kScan) {
-    float vv[kScan];
-    int ii[kScan];
-#pragma unroll
-    for (int u = 0; u < kScan; ++u) {
-      const int e = e0 + u * blockDim.x + threadIdx.x;
-      vv[u] = -INFINITY;
-      ii[u] = 0x7fffffff;
-      if (e < M * n) cand(e / n, e % n, vv[u], ii[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < kScan; ++u) {
-      const int e = e0 + u * blockDim.x + threadIdx.x;
-      if (e < M * n) {
-        const int t = e / n;
-        if (!beats(thv[t], thi[t], vv[u], ii[u])) {
-          const int pos = atomicAdd(&cnt[t], 1);
-          if (pos < kMergeCap) { cv_s[t * kMergeCap + pos] = vv[u]; ci_s[t * kMergeCap + pos] = ii[u]; }
+        for (int hr = 0; hr < 2; ++hr) {
+          const bool mine = (q == (t8 >> 1)) && (hr ? vb_ok : va_ok);
+          const float val = lg[2 * hr + (t8 & 1)];
+          const int idx = (int)(vt + g + 8 * hr);
+          unsigned m = __ballot_sync(0xffffffffu, mine && beats(val, idx, lst[t].thr_v, lst[t].thr_i));
+          while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const float bv = __shfl_sync(0xffffffffu, val, src);
+            const int bi = __shfl_sync(0xffffffffu, idx, src);
+            list_insert(lst[t], bv, bi, tk, lane);
+          }
         }
       }
     }
+  };
+
+  float acc[NT][STEPS][4];
+  float part0[NT][4], part1[NT][4];                   // partial sums of this warp's cut first / last tile
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) part0[nt][j] = part1[nt][j] = 0.f;
+  const uint8_t* pa = nullptr;
+  const uint8_t* pb = nullptr;
+  bool va_ok = false, vb_ok = false;
+  for (int u = u0; u < u1; ++u) {
+    const int tl = u / NG, gi = u % NG;
+    if (u == u0 || gi == 0) {                          // a tile starts (or this warp's range does)
+      const long long vt = v0 + 16LL * tl;
+      va_ok = vt + g < v1;
+      vb_ok = vt + g + 8 < v1;
+      pa = p.w + (vt + g) * ROWB + 16 * q;
+      pb = p.w + (vt + g + 8) * ROWB + 16 * q;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int s2 = 0; s2 < STEPS; ++s2)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[nt][s2][j] = 0.f;
+    }
+    if (MDW_HEAD_PF > 0) prefetch_unit(u + MDW_HEAD_PF);
+    uint4 wa[U], wb[U];
+#pragma unroll
+    for (int c = 0; c < U; ++c) {
+      const int off = 64 * (gi * U + c);
+      wa[c] = va_ok ? ldg_stream16(pa + off) : make_uint4(0, 0, 0, 0);
+      wb[c] = vb_ok ? ldg_stream16(pb + off) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < U; ++c) {
+      const int ch = gi * U + c;
+      const uint32_t A[4] = {wa[c].x, wa[c].y, wa[c].z, wa[c].w};
+      const uint32_t B[4] = {wb[c].x, wb[c].y, wb[c].z, wb[c].w};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int tok = 8 * nt + g;
+        const bool have = tok < M;
+        const uint8_t* xt = xsm + (size_t)tok * XS;
+        if (FP8) {
+          uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+          if (have) {
+            x0 = *reinterpret_cast<const uint4*>(xt + 2 * (64 * ch + 16 * q));
+            x1 = *reinterpret_cast<const uint4*>(xt + 2 * (64 * ch + 16 * q) + 16);
+          }
+          const uint32_t X[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int s2 = 0; s2 < STEPS; ++s2)
+            mma_f16_16816(acc[nt][s2], e4m3x2_to_f16x2(A[s2] & 0xFFFF), e4m3x2_to_f16x2(B[s2] & 0xFFFF),
+                          e4m3x2_to_f16x2(A[s2] >> 16), e4m3x2_to_f16x2(B[s2] >> 16), X[2 * s2], X[2 * s2 + 1]);
+        } else {
+          uint4 x0 = make_uint4(0, 0, 0, 0);
+          if (have) x0 = *reinterpret_cast<const uint4*>(xt + 64 * ch + 16 * q);
+          const uint32_t X[4] = {x0.x, x0.y, x0.z, x0.w};
+#pragma unroll
+          for (int s2 = 0; s2 < STEPS; ++s2)
+            mma_bf16_16816(acc[nt][s2], A[2 * s2], B[2 * s2], A[2 * s2 + 1], B[2 * s2 + 1], X[2 * s2], X[2 * s2 + 1]);
+        }
+      }
+    }
+    if (gi == NG - 1 || u == u1 - 1) {                 // a tile ends (or this warp's range does)
+      float d[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float v = acc[nt][0][j];
+#pragma unroll
+          for (int s2 = 1; s2 < STEPS; ++s2) v += acc[nt][s2][j];
+          d[nt][j] = v;
+        }
+      if (tl * NG >= u0 && gi == NG - 1) {
+        finish_tile(tl, d);                            // the whole tile is this warp's
+      } else if (tl == u0 / NG) {                      // first tile, cut at one end or both
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) part0[nt][j] = d[nt][j];
+      } else {                                         // last tile, cut at the range's end
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) part1[nt][j] = d[nt][j];
+      }
+    }
+  }
+  MDW_HEAD_TRACE(lane == 0, 8 + warp);
+  __syncthreads();                                     // the hidden states are dead from here on
+  MDW_HEAD_TRACE(threadIdx.x == 0, 2);
+
+  // tiles cut between warps: every warp leaves its cut first / last tile's partial sums in
+  // shared memory; the warp holding a cut tile's first unit adds the later warps' parts in
+  // K order and finishes the tile
+  const bool nonempty = u0 < u1;
+  const int tF = u0 / NG, tL = nonempty ? (u1 - 1) / NG : tF;
+  auto rec_at = [&](int w, int side, int nt) {
+    return reinterpret_cast<float4*>(rec + ((size_t)((w * 2 + side) * NT + nt) * 32 + lane) * 4);
+  };
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    *rec_at(warp, 0, nt) = make_float4(part0[nt][0], part0[nt][1], part0[nt][2], part0[nt][3]);
+    *rec_at(warp, 1, nt) = make_float4(part1[nt][0], part1[nt][1], part1[nt][2], part1[nt][3]);
   }
   __syncthreads();
-  // C. warp t selects token t's top-tk (rescans global memory only on a compaction overflow)
-  for (int t = warp; t < M; t += kWarps) {
-    float* outv = ov + t * kMaxTK;
-    int* outi = oi + t * kMaxTK;
-    if (cnt[t] <= kMergeCap) {
-      auto ld = [&](int k, float& vv, int& ii) { vv = cv_s[t * kMergeCap + k]; ii = ci_s[t * kMergeCap + k]; };
-      warp_topk(ld, cnt[t], tk, thv[t], thi[t], tv_s + warp * kMergeCap, ti_s + warp * kMergeCap, kMergeCap,
-                outv, outi, lane);
-    } else {
-      auto ld = [&](int k, float& vv, int& ii) { cand(t, k, vv, ii); };
-      warp_topk(ld, n, tk, thv[t], thi[t], tv_s + warp * kMergeCap, ti_s + warp * kMergeCap, kMergeCap,
-                outv, outi, lane);
+  MDW_HEAD_TRACE(threadIdx.x == 0, 16);
+  if (nonempty && tL * NG >= u0 && (tL + 1) * NG > u1) {
+    float d[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[nt][j] = (tL == tF) ? part0[nt][j] : part1[nt][j];
+    for (int w2 = warp + 1; w2 < kWarps && ubeg(w2) < (tL + 1) * NG; ++w2) {
+      if (ubeg(w2) == ubeg(w2 + 1)) continue;          // empty range
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float4 r = *rec_at(w2, 0, nt);           // tile tL is w2's first tile
+        d[nt][0] += r.x; d[nt][1] += r.y; d[nt][2] += r.z; d[nt][3] += r.w;
+      }
     }
-    for (int r = lane; r < tk; r += 32) {
-      if (r == 0) p.argmax_out[t] = outi[0];
-      if (p.topk_idx) p.topk_idx[(size_t)t * tk + r] = outi[r];
-      if (p.topk_val) p.topk_val[(size_t)t * tk + r] = outv[r];
-    }
+    finish_tile(tL, d);
   }
+
+  // block list of every token: the warps' lists, tree-merged
+#pragma unroll
+  for (int t = 0; t < MAXM; ++t)
+    if (t < M) {
+      lv[(t * kWarps + warp) * kMaxTK + lane] = lst[t].v;
+      li[(t * kWarps + warp) * kMaxTK + lane] = lst[t].i;
+    }
+#ifdef MDW_TRACE
+  __syncthreads();
+  MDW_HEAD_TRACE(threadIdx.x == 0, 17);
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_head_trace[blockIdx.x * 24 + 20] = smid;
+  }
+#endif
+  tree_merge(lv, li, M, warp, lane);
+  MDW_HEAD_TRACE(threadIdx.x == 0, 18);
+  for (int t = warp; t < M; t += kWarps)
+    if (lane < tk) {
+      const size_t o = ((size_t)blockIdx.x * M + t) * tk + lane;
+      p.cand_val[o] = lv[t * kWarps * kMaxTK + lane];
+      p.cand_idx[o] = li[t * kWarps * kMaxTK + lane];
+    }
+  MDW_HEAD_TRACE(threadIdx.x == 0, 3);
+
+  // the last block of each group of kHeadGroupSize blocks merges the group's lists; the last
+  // group to finish merges the group lists into the result
+  __threadfence();
+  __syncthreads();
+  const int grp = blockIdx.x / kHeadGroupSize;
+  const int gfirst = grp * kHeadGroupSize;
+  const int gn = min((int)G - gfirst, kHeadGroupSize);
+  if (threadIdx.x == 0) is_last = (atomicAdd(p.hdr + kHdrHeadGroups + grp, 1u) == (uint32_t)(gn - 1));
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  MDW_HEAD_TRACE(threadIdx.x == 0, 4);
+  merge_global_lists<MAXM>(p.cand_val, p.cand_idx, gfirst, gn, M, tk, lv, li, warp, lane);
+  float* gcv = p.cand_val + (size_t)G * M * tk;
+  int* gci = p.cand_idx + (size_t)G * M * tk;
+  for (int t = warp; t < M; t += kWarps)
+    if (lane < tk) {
+      const size_t o = ((size_t)grp * M + t) * tk + lane;
+      gcv[o] = lv[t * kWarps * kMaxTK + lane];
+      gci[o] = li[t * kWarps * kMaxTK + lane];
+    }
+  __threadfence();
+  __syncthreads();
+  const int ngroups = (int)((G + kHeadGroupSize - 1) / kHeadGroupSize);
+  if (threadIdx.x == 0) is_last = (atomicAdd(p.hdr + kHdrDoneCtr, 1u) == (uint32_t)(ngroups - 1));
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  MDW_HEAD_TRACE(threadIdx.x == 0, 5);
+  merge_global_lists<MAXM>(gcv, gci, 0, ngroups, M, tk, lv, li, warp, lane);
+  for (int t = warp; t < M; t += kWarps)
+    if (lane < tk) {
+      const float v = lv[t * kWarps * kMaxTK + lane];
+      const int i = li[t * kWarps * kMaxTK + lane];
+      if (lane == 0) p.argmax_out[t] = i;
+      if (p.topk_idx) p.topk_idx[(size_t)t * tk + lane] = i;
+      if (p.topk_val) p.topk_val[(size_t)t * tk + lane] = v;
+    }
+  MDW_HEAD_TRACE(threadIdx.x == 0, 6);
 }
 
 template <bool FP8, int MAXM>
 cudaError_t launch_head_t(const HeadParams& p, cudaStream_t s) {
-  const size_t smem = head_smem_bytes(p.M, MAXM);
+  const size_t smem = head_smem_bytes(p.M, MAXM, head_x_stride<FP8>());
   auto kern = head_kernel<FP8, MAXM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -459,7 +636,7 @@ cudaError_t launch_head_any(const HeadParams& p, cudaStream_t s) {
 }  // namespace
 
 size_t head_ws_bytes(int M, int topk, int grid) {
-  return (size_t)grid * M * topk * 8 + 512;
+  return (size_t)(grid + kHeadMaxGroups) * M * topk * 8 + 512;
 }
 
 cudaError_t launch_head_fp8(const HeadParams& p, cudaStream_t s) { return launch_head_any<true>(p, s); }
@@ -473,3 +650,10 @@ cudaError_t launch_quantize_head(const __nv_bfloat16* w, long long V, uint8_t* q
 }
 
 }  // namespace mdw
+
+#ifdef MDW_TRACE
+extern "C" int mdw_head_trace_read(void* host, size_t bytes) {
+  if (bytes > sizeof(mdw::g_head_trace)) bytes = sizeof(mdw::g_head_trace);
+  return cudaMemcpyFromSymbol(host, mdw::g_head_trace, bytes) == cudaSuccess ? 0 : -1;
+}
+#endif

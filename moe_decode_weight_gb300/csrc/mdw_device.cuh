@@ -31,7 +31,8 @@ enum HeaderWord : int {
   kHdrSlots = 2,      // S: expert slots of the last layer
   kHdrPairs = 3,      // P: (token, expert) pairs of the last layer
   kHdrRouted = 4,     // routed slots of the last layer
-  kHdrDoneCtr = 5,    // last-block-done counter of the LM head
+  kHdrDoneCtr = 5,    // last-group-done counter of the LM head
+  kHdrHeadGroups = 16,  // [16 + g]: blocks of LM-head group g done (16 words)
   kHdrUnions = 64,    // [64 + l]: routed union size of layer l (stack)
   kHdrWords = 256
 };

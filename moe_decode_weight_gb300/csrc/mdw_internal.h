@@ -63,6 +63,12 @@ struct MoeParams {
   float* sh;                   // [P]
 };
 
+// The LM head's cross-block merge: blocks form groups of kHeadGroupSize; each group's last
+// block merges the group's lists, the last group merges the group lists.
+constexpr int kHeadGroupSize = 16;
+constexpr int kHeadMaxGroups = 16;
+constexpr int kMaxHeadGrid = kHeadGroupSize * kHeadMaxGroups;   // blocks of the head kernel (<= 256)
+
 struct HeadParams {
   const uint8_t* w;            // [V][H] E4M3 or bf16 (as bytes)
   const float* row_scale;      // [V] or null (bf16)
@@ -76,8 +82,8 @@ struct HeadParams {
   int32_t* topk_idx;           // [M][topk] or null
   float* topk_val;             // [M][topk] or null
   uint32_t* hdr;               // header (status, done counter)
-  float* cand_val;             // [grid][M][topk]
-  int32_t* cand_idx;           // [grid][M][topk]
+  float* cand_val;             // [grid + kHeadMaxGroups][M][topk]: block lists, then group lists
+  int32_t* cand_idx;           // [grid + kHeadMaxGroups][M][topk]
 };
 
 // Workspace layout helpers (host).
