@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
         const bool okr = (j < 2) ? va_ok : vb_ok;
         lg[j] = d[nt][j] * ((j < 2) ? sa : sb) * (tok < M ? xmul[tok] : 1.0f);
         if (p.logits && okr && tok < M) p.logits[(size_t)tok * p.V + vt + g + ((j >> 1) << 3)] = lg[j];
+        if (lg[j] != lg[j]) lg[j] = -INFINITY;         // a NaN logit ranks last in the top-k
       }
 #pragma unroll
       for (int t8 = 0; t8 < 8; ++t8) {

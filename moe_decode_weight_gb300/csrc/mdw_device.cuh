@@ -97,6 +97,27 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
   return r;
 }
+// Four E2M1 code pairs (the four bytes of w, byte 0 first) -> four f16x2 (exact).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+      " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// E8M0 scales whose power of two, applied to any E2M1 value in f16, stays exact: s in
+// [113, 140] gives 2^-14 .. 2^13 (a normal f16), and every product E2M1 x 2^(s-127) lies in
+// [2^-15, 6 * 2^13], a multiple of 2^-24 below 65504. All four bytes of `four` checked.
+__device__ __forceinline__ bool e8m0x4_f16_exact(uint32_t four) {
+  return __vcmpleu4(__vsub4(four, 0x71717171u), 0x1B1B1B1Bu) == 0xFFFFFFFFu;
+}
+// f16x2 with 2^(s-127) in both halves, for s in [113, 140] (exponent field s - 112).
+__device__ __forceinline__ uint32_t e8m0_to_f16x2_pow2(uint32_t s) { return (s - 112u) * 0x04000400u; }
+
 // E8M0 scale byte -> fp32 2^(s-127) (s = 0 gives 2^-127, a subnormal; 255 gives NaN).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
   return s == 0 ? __uint_as_float(0x00400000u) : (s == 255 ? __uint_as_float(0x7FC00000u)

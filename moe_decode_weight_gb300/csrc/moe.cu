@@ -41,6 +41,7 @@ constexpr int kW2RowBytes = kI / 2;             // 384
 constexpr int kXhBytes = kH * 2 + 64;           // f16 x-hat per token, padded (conflict-free B loads)
 constexpr int kGuRound = 4 * kWarps;            // gate/up units per round (partials in smem)
 constexpr int kGuMaxTiles = 320;                // (tile, token-tile) entries per block
+constexpr int kMaxSegs = 32;                    // slot segments per block list
 constexpr int kTopkCand = 128;                  // compacted top-k candidates per warp
 constexpr int kHhBytes = kI * 2 + 64;           // f16 h-hat per pair, padded (conflict-free A loads)
 constexpr int kPairChunk = 24;                  // pairs quantised into smem at a time
@@ -52,22 +53,33 @@ constexpr int kGuStageBytes = 16 * kGuPitch + 16 * kGuU;
 constexpr int kDnStages = 2;                    // down: 16 W2 rows x 12 blocks per stage
 constexpr int kDnKB = kIBlocks / 2;             // blocks per K half (12)
 constexpr int kDnPitch = kDnKB * 16 + 16;       // 208 bytes: conflict-free fragment reads
+constexpr int kDnBcPitch = kDnKB * 16;          // 192 bytes (= 64 mod 128): conflict-free 16-byte reads
 constexpr int kDnStageBytes = 16 * kDnPitch + 16 * kIBlocks;
 constexpr int kWarpRing = (kGuStages * kGuStageBytes > kDnStages * kDnStageBytes)
                               ? kGuStages * kGuStageBytes : kDnStages * kDnStageBytes;
+// block-column form (M <= 2): unpadded 128-byte rows (swizzled chunks); the same depth as
+// the token-column ring (a deeper ring measured slower: more requests in flight per SM
+// delayed the first stages)
+constexpr int kGuBcStages = 3;
+constexpr int kGuBcStageBytes = 16 * kGuU * 16 + 16 * kGuU;
+constexpr int kWarpRingBc = (kGuBcStages * kGuBcStageBytes > kDnStages * kDnStageBytes)
+                                ? kGuBcStages * kGuBcStageBytes : kDnStages * kDnStageBytes;
+__host__ __device__ constexpr int warp_ring_bytes(int M) { return M <= 2 ? kWarpRingBc : kWarpRing; }
 constexpr int kMaxRowsPerBlock = 32;            // down-projection rows per block (>= H / grid)
 
 // ------------------------------------------------------------------ phase trace
 
+constexpr int kTraceNone = -1;
+
 // Built only with -DMDW_TRACE (a profiling build of the library, never the product build):
 // thread 0 of every block records %globaltimer at each phase boundary of every layer.
 #ifdef MDW_TRACE
-constexpr int kTracePhases = 16;
+constexpr int kTracePhases = 20;
 constexpr int kTraceLayers = 64;
 __device__ unsigned long long g_trace[kTraceLayers * kTracePhases * 256];
 #define MDW_TRACE_POINT(layer, phase)                                                        \
   do {                                                                                       \
-    if (threadIdx.x == 0 && (layer) < kTraceLayers) {                                        \
+    if (threadIdx.x == 0 && (layer) >= 0 && (layer) < kTraceLayers) {                                        \
       unsigned long long t_;                                                                 \
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                 \
       g_trace[((layer) * kTracePhases + (phase)) * 256 + blockIdx.x] = t_;                   \
@@ -86,8 +98,8 @@ __host__ __device__ inline Smem smem_layout(int M) {
   Smem s;
   const size_t r1 = (size_t)M * kXhBytes > (size_t)kPairChunk * kHhBytes ? (size_t)M * kXhBytes
                                                                           : (size_t)kPairChunk * kHhBytes;
-  const size_t r2 = (size_t)M * kH * 2 > (size_t)kWarps * kWarpRing ? (size_t)M * kH * 2
-                                                                     : (size_t)kWarps * kWarpRing;
+  const size_t rings = (size_t)kWarps * warp_ring_bytes(M);
+  const size_t r2 = (size_t)M * kH * 2 > rings ? (size_t)M * kH * 2 : rings;
   s.xh = 0;
   s.hh = 0;
   s.xb = (r1 + 127) & ~(size_t)127;
@@ -119,6 +131,8 @@ struct Tables {
   float sh[kPairChunk];
   int n_slots, n_routed, n_pairs, shared_slot, bad;
   int gu_n;                                    // entries in gu_tile
+  int n_segs;                                  // slot segments of the block's gate/up share
+  int seg_slot[kMaxSegs], seg_lo[kMaxSegs], seg_hi[kMaxSegs], seg_groups[kMaxSegs], seg_off[kMaxSegs + 1];
   int4 gu_tile[kGuMaxTiles];                   // (slot, j0, rows, first token column)
 };
 static_assert(sizeof(Tables) <= 12288, "tables exceed the reserved shared memory");
@@ -218,16 +232,27 @@ __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tabl
 
 // ------------------------------------------------------------------ P1: router rows
 
-__device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_t* smem) {
-  const int M = p.M, E = p.E, G = gridDim.x;
-  const int e0 = (int)((long long)blockIdx.x * E / G), e1 = (int)((long long)(blockIdx.x + 1) * E / G);
+// The block's router rows [e0, e1): warp w takes rows e0 + w, e0 + w + warps, ...; the first
+// row's weights are loaded (into `wv`) before the input is ready, by load_router_row.
+__device__ __forceinline__ void router_range(const MoeParams& p, int& e0, int& e1) {
+  const int G = gridDim.x;
+  e0 = (int)((long long)blockIdx.x * p.E / G);
+  e1 = (int)((long long)(blockIdx.x + 1) * p.E / G);
+}
+__device__ __forceinline__ void load_router_row(const LayerDesc& L, int e, uint4 (&wv)[10]) {
+  const uint4* wr = reinterpret_cast<const uint4*>(L.router_w + (size_t)e * kH);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) wv[i] = ldg_stream16(wr + 32 * i + lane);
+}
+__device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, uint4 (&wv)[10]) {
+  const int M = p.M, E = p.E;
+  int e0, e1;
+  router_range(p, e0, e1);
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem + smem_layout(M).xb);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = e0 + warp; e < e1; e += kWarps) {
-    const uint4* wr = reinterpret_cast<const uint4*>(L.router_w + (size_t)e * kH);
-    uint4 wv[10];
-#pragma unroll
-    for (int i = 0; i < 10; ++i) wv[i] = ldg_stream16(wr + 32 * i + lane);
+    if (e != e0 + warp) load_router_row(L, e, wv);
     for (int t = 0; t < M; ++t) {
       const uint4* x4 = reinterpret_cast<const uint4*>(xb + (size_t)t * kH);
       float acc = 0.f;
@@ -250,7 +275,9 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
 
 // ------------------------------------------------------------------ P2: top-k + dedup
 
-__device__ void route_tokens(const MoeParams& p, Tables& tb, int layer, uint8_t* scratch) {
+__device__ void prefetch_block_weights(const MoeParams& p, const LayerDesc& L, const Tables& tb, int a, int b);
+
+__device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb, int layer, uint8_t* scratch) {
   const int M = p.M, E = p.E, K = p.K;
   // per-warp candidate buffers live in the gate/up partial-sum region (not live during
   // routing)
@@ -288,6 +315,7 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb, int layer, uint8_t*
       for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
         v[j] = e < E ? ld_cg_f32(z + e) : -INFINITY;
+        if (v[j] != v[j]) v[j] = -INFINITY;            // a NaN logit ranks last (ids stay valid)
         if (e < E && beats(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
       }
       // bitonic sort of (bv, bi), descending in `beats` order
@@ -350,29 +378,49 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb, int layer, uint8_t*
   __syncthreads();
   MDW_TRACE_POINT(layer, 10);
   if (tb.bad) return;
-  // Routing tables, built by warp 0 alone: gates, the union of the selections, slots
-  // (slot 0 = shared expert when present, then the union ascending) and the pairs
-  // (slot-major, token-minor).
+  // Routing tables (warp 0): gates, the union of the selections and its slots (slot 0 = shared
+  // expert when present, then the union ascending); then the pairs (slot-major,
+  // token-minor). Between the two, the block's gate/up share is known, and the other warps
+  // ask L2 for its weights while warp 0 finishes the pair tables.
+  const int first = p.has_shared ? 1 : 0;
+  auto slot_of = [&](int e) {
+    return first + tb.wpre[e >> 5] + __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
+  };
   if (warp == 0) {
-    // gates: softmax over each token's selected logits, one (token, rank) per lane
-    for (int i = lane; i < M * K; i += 32) {
-      const int t = i / K;
-      const float* z = tb.gts + t * K;
-      float mx = z[0];
-      for (int r = 1; r < K; ++r) mx = fmaxf(mx, z[r]);
-      float sum = 0.f;
-      for (int r = 0; r < K; ++r) sum += expf(z[r] - mx);
-      tb.cand_g[i] = expf(z[i % K] - mx) / sum;
+    // gates: softmax over each token's K selected logits, one (token, rank) per lane
+    const bool pow2 = (K & (K - 1)) == 0;             // then a token's K entries share K aligned lanes
+    for (int i0 = 0; i0 < M * K; i0 += 32) {
+      const int i = i0 + lane;
+      const bool act = i < M * K;
+      float gate = 0.f;
+      if (pow2) {
+        const float z = act ? tb.gts[i] : 0.f;
+        float mx = z;
+        for (int o = 1; o < K; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float ez = expf(z - mx);
+        float sum = ez;
+        for (int o = 1; o < K; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        gate = ez / sum;
+      } else if (act) {
+        const float* z = tb.gts + (i / K) * K;
+        float mx = z[0];
+        for (int r = 1; r < K; ++r) mx = fmaxf(mx, z[r]);
+        float sum = 0.f;
+        for (int r = 0; r < K; ++r) sum += expf(z[r] - mx);
+        gate = expf(z[i % K] - mx) / sum;
+      }
+      if (act) tb.cand_g[i] = gate;
     }
-    __syncwarp();
-    for (int i = lane; i < M * K; i += 32) tb.gts[i] = tb.cand_g[i];
     if (lane < MDW_MAX_EXPERTS / 32) tb.bitmap[lane] = 0;
     __syncwarp();
-    for (int i = lane; i < M * K; i += 32) atomicOr(&tb.bitmap[tb.ids[i] >> 5], 1u << (tb.ids[i] & 31));
+    for (int i = lane; i < M * K; i += 32) {
+      tb.gts[i] = tb.cand_g[i];
+      atomicOr(&tb.bitmap[tb.ids[i] >> 5], 1u << (tb.ids[i] & 31));
+    }
     __syncwarp();
-    const int first = p.has_shared ? 1 : 0;
     const uint32_t word = lane < MDW_MAX_EXPERTS / 32 ? tb.bitmap[lane] : 0u;
-    int cnt = __popc(word), incl = cnt;
+    const int cnt = __popc(word);
+    int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int nb = __shfl_up_sync(0xffffffffu, incl, o);
@@ -381,27 +429,30 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb, int layer, uint8_t*
     if (lane < MDW_MAX_EXPERTS / 32) tb.wpre[lane] = incl - cnt;
     int pos = first + incl - cnt;
     for (uint32_t w = word; w; w &= w - 1) {
-      tb.cnt[pos] = 0;
+      tb.cnt[pos] = 0;                                  // token masks of the routed slots
       tb.slot_expert[pos++] = lane * 32 + __ffs(w) - 1;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
-    const int S = total + first;
     if (lane == 0) {
       tb.n_routed = total;
-      tb.n_slots = S;
+      tb.n_slots = total + first;
       tb.shared_slot = p.has_shared ? 0 : -1;
-      if (p.has_shared) { tb.slot_expert[0] = -1; tb.cnt[0] = M; }
+      if (p.has_shared) tb.slot_expert[0] = -1;
     }
-    __syncwarp();
-    auto slot_of = [&](int e) {
-      return first + tb.wpre[e >> 5] + __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-    };
-    for (int i = lane; i < M * K; i += 32) atomicAdd(&tb.cnt[slot_of(tb.ids[i])], 1);
+  }
+  __syncthreads();
+  MDW_TRACE_POINT(layer, 11);
+  const int S = tb.n_slots;
+  if (warp == 0) {
+    // token masks of the routed slots -> counts -> slot_begin (scan) -> pair positions: the
+    // pairs of a slot are token-ordered, so a pair's rank is the number of the slot's earlier
+    // tokens, popc(mask & ((1 << t) - 1))
+    for (int i = lane; i < M * K; i += 32) atomicOr(reinterpret_cast<unsigned*>(&tb.cnt[slot_of(tb.ids[i])]), 1u << (i / K));
     __syncwarp();
     int carry = 0;
     for (int b0 = 0; b0 < S; b0 += 32) {
       const int sidx = b0 + lane;
-      const int c = sidx < S ? tb.cnt[sidx] : 0;
+      const int c = sidx < S ? (sidx < first ? M : __popc((unsigned)tb.cnt[sidx])) : 0;
       int in2 = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -414,20 +465,20 @@ __device__ void route_tokens(const MoeParams& p, Tables& tb, int layer, uint8_t*
     if (lane == 0) { tb.slot_begin[S] = carry; tb.n_pairs = carry; }
     __syncwarp();
     for (int i = lane; i < M * K; i += 32) {
-      const int t = i / K, e = tb.ids[i];
-      int rank = 0;
-      for (int t2 = 0; t2 < t; ++t2)
-        for (int r2 = 0; r2 < K; ++r2) rank += (tb.ids[t2 * K + r2] == e);
-      const int sidx = slot_of(e), q = tb.slot_begin[sidx] + rank;
+      const int t = i / K, sidx = slot_of(tb.ids[i]);
+      const int q = tb.slot_begin[sidx] + __popc((unsigned)tb.cnt[sidx] & ((1u << t) - 1u));
       tb.pair_token[q] = t;
       tb.pair_slot[q] = sidx;
       tb.pair_gate[q] = tb.gts[i];
     }
     if (p.has_shared)
       for (int t = lane; t < M; t += 32) { tb.pair_token[t] = t; tb.pair_slot[t] = 0; tb.pair_gate[t] = 1.0f; }
+  } else {
+    const long long PR = (long long)S * kI;
+    const int G = gridDim.x;
+    prefetch_block_weights(p, L, tb, (int)((long long)blockIdx.x * PR / G), (int)((long long)(blockIdx.x + 1) * PR / G));
   }
   __syncthreads();
-  MDW_TRACE_POINT(layer, 11);
   if (blockIdx.x == 0) {
     // publish the routing (inspection + optional outputs)
     for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
@@ -473,54 +524,164 @@ __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-// One MMA tile of the gate/up GEMVs: rows 0..7 of the MMA = gate rows j0..j0+7 and rows
-// 8..15 = the matching up rows of one expert; columns = 8 tokens of the slot; K = blocks
-// [kb0, kb1) of 32 (a multiple of kGuU). The weight rows stream through the warp's
-// cp.async ring (kGuStages stages of kGuU blocks x 16 rows, rows padded so the fragment
-// reads are bank-conflict free). Each 32-block is two k16 MMAs on a permuted K order: lane
+// ---- block-column MMA steps (at most two tokens per MMA tile) ----
+// With one or two tokens, most of an m16n8 tile's eight columns would be idle. Instead the
+// columns carry (token, block) pairs: column c = token c >> 2, block c & 3 of a four-block
+// super-step. Lane (g, q) holds the whole 16-byte block sb + q of rows g and g + 8, so its
+// k positions of every MMA come from that block; the B operand of column c is the token's
+// x-hat on block sb + (c & 3) and zero elsewhere, so column c collects the (unscaled) dot
+// product of each row with one block, and each lane scales its own columns by the rows'
+// E8M0 scales in fp32. The MMAs need no per-block fresh accumulator and the weights no
+// scaling, so the step costs about half the instructions of the token-column form.
+//
+// bc_step: wr0 / wr1 = block sb + q of rows g and g + 8; xb = the x-hat (f16, natural order)
+// of token g >> 2 on block sb + q when q == (g & 3), else null. Adds the partial dots of the
+// lane's columns 2q, 2q + 1 (token q >> 1, blocks sb + 2 (q & 1) + {0, 1}) into d.
+__device__ __forceinline__ void bc_step(uint4 wr0, uint4 wr1, const uint8_t* xb, float (&d)[4]) {
+  const uint32_t A[4] = {wr0.x, wr0.y, wr0.z, wr0.w}, B[4] = {wr1.x, wr1.y, wr1.z, wr1.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint4 xv = make_uint4(0, 0, 0, 0);
+    if (xb) xv = *reinterpret_cast<const uint4*>(xb + 16 * w);
+    uint32_t ha[4], hb[4];
+    e2m1x8_to_f16x2x4(A[w], ha);
+    e2m1x8_to_f16x2x4(B[w], hb);
+    mma_16816(d, ha[0], hb[0], ha[1], hb[1], xv.x, xv.y);
+    mma_16816(d, ha[2], hb[2], ha[3], hb[3], xv.z, xv.w);
+  }
+}
+// acc[0] (row g) and acc[1] (row g + 8) += the lane's two columns scaled by the rows' E8M0
+// scales of those blocks (sa0/sa1: row g, blocks 2 (q & 1) + {0, 1} of the super-step; sb0 /
+// sb1: row g + 8).
+__device__ __forceinline__ void bc_scale_add(const float (&d)[4], uint32_t sa0, uint32_t sa1, uint32_t sb0,
+                                             uint32_t sb1, float (&acc)[2]) {
+  acc[0] = fmaf(e8m0_to_f32(sa0), d[0], acc[0]);
+  acc[0] = fmaf(e8m0_to_f32(sa1), d[1], acc[0]);
+  acc[1] = fmaf(e8m0_to_f32(sb0), d[2], acc[1]);
+  acc[1] = fmaf(e8m0_to_f32(sb1), d[3], acc[1]);
+}
+// End of a block-column unit: the lane pairs (q, q ^ 1) add their blocks, then lane q == 0
+// collects token 1 from lane 2, giving the token-column layout of an m16n8 result:
+// r = {row g token 0, row g token 1, row g+8 token 0, row g+8 token 1} on lane q == 0, zeros
+// on the other lanes (their columns would be tokens >= 2).
+__device__ __forceinline__ void bc_finish(const float (&acc)[2], int q, float (&r)[4]) {
+  const float a0 = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 1);
+  const float a1 = acc[1] + __shfl_xor_sync(0xffffffffu, acc[1], 1);
+  const float t0 = __shfl_xor_sync(0xffffffffu, a0, 2);
+  const float t1 = __shfl_xor_sync(0xffffffffu, a1, 2);
+  const bool own = (q == 0);
+  r[0] = own ? a0 : 0.f;
+  r[1] = own ? t0 : 0.f;
+  r[2] = own ? a1 : 0.f;
+  r[3] = own ? t1 : 0.f;
+}
+
+// One gate/up unit: MMA rows 0..7 = gate rows j0..j0+7 and rows 8..15 = the matching up rows
+// of one expert; columns = 8 tokens of the slot (xtok = this lane's token's x-hat, or null);
+// K = spu stages of kGuU blocks of 32 from block kb0.
+struct GuUnit {
+  const uint8_t* q13;
+  const uint8_t* s13;
+  const uint8_t* xtok;
+  int j0, nr, kb0;
+};
+
+// A warp's n gate/up units as one continuous pipeline: the weight rows of every stage stream
+// through the warp's cp.async ring (STAGES stages of kGuU blocks x 16 rows, rows padded so
+// the fragment reads are bank-conflict free), the next unit's stages being requested while
+// the current one is computed. Each 32-block is two k16 MMAs on a permuted K order: lane
 // (g, q) feeds bytes 4q..4q+3 of the block (E2M1 pairs, via cvt.e2m1x2) as its A registers
-// and the matching x-hat values 8q..8q+7 (one 16-byte load) as its B registers; the block's
-// fresh fp32 result is scaled by its E8M0 scale (per row) into the accumulator:
+// and the matching x-hat values 8q..8q+7 (one 16-byte load) as its B registers. When every
+// E8M0 scale of a stage keeps E2M1 x 2^(s-127) exact in f16, the scale is multiplied into the
+// f16 weights and the MMAs accumulate straight into fp32 (even and odd blocks in two
+// accumulators); otherwise each block's fresh fp32 result is scaled in fp32 and added. At the
+// end of unit j, done(j, acc) receives
 //   acc[0..1] = gate rows g, tokens 2q..2q+1;  acc[2..3] = up rows g, same tokens.
-__device__ __forceinline__ void gate_up_tile(const uint8_t* q13, const uint8_t* s13, int j0, int nr,
-                                             const uint8_t* xtok, int kb0, int kb1, float (&acc)[4],
-                                             uint8_t* ring, int lane) {
+template <bool BC, typename Info, typename Done>
+__device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done done, uint8_t* ring, int lane) {
+  constexpr int STAGES = BC ? kGuBcStages : kGuStages;
+  constexpr int SBYTES = BC ? kGuBcStageBytes : kGuStageBytes;
   const int g = lane >> 2, q = lane & 3;
-  const bool rv = g < nr;
-  const int nst = (kb1 - kb0) / kGuU;
+  const int total = n * spu;
+  // unit descriptors held in registers: the one being requested and the one being computed
+  GuUnit Ui, Uc;
+  int ji = -1, jc = -1;
   auto issue = [&](int st) {
-    uint8_t* dst = ring + (st % kGuStages) * kGuStageBytes;
-    const int bb = kb0 + st * kGuU;
+    if (st / spu != ji) { ji = st / spu; Ui = info(ji); }
+    const GuUnit& U = Ui;
+    uint8_t* dst = ring + (st % STAGES) * SBYTES;
+    const int bb = U.kb0 + (st % spu) * kGuU;
+    // token-column layout: rows of kGuPitch bytes (padded for the 4-byte fragment reads);
+    // block-column layout: rows of 128 bytes, chunk b of row r at b ^ 4 (r & 1), so the
+    // 16-byte reads of lanes (g, q) (rows g, chunks sb + q) hit distinct banks
+    constexpr int pitch = BC ? kGuU * 16 : kGuPitch;
 #pragma unroll
     for (int k = 0; k < 16 * kGuU / 32; ++k) {        // 16 rows x kGuU chunks of 16 bytes
       const int c = lane + 32 * k, row = c / kGuU, blk = c % kGuU, rr = row & 7;
-      if (rr < nr) {
-        const size_t grow = (size_t)(row < 8 ? j0 + rr : kI + j0 + rr);
-        cp_async16(dst + row * kGuPitch + blk * 16, q13 + grow * kW13RowBytes + (bb + blk) * 16);
+      if (rr < U.nr) {
+        const size_t grow = (size_t)(row < 8 ? U.j0 + rr : kI + U.j0 + rr);
+        const int pos = BC ? (blk ^ ((row & 1) << 2)) : blk;
+        cp_async16(dst + row * pitch + pos * 16, U.q13 + grow * kW13RowBytes + (bb + blk) * 16);
       }
     }
-    if (lane < 16 && (lane & 7) < nr) {                // 16 rows x kGuU scale bytes
-      const size_t grow = (size_t)(lane < 8 ? j0 + lane : kI + j0 + (lane & 7));
-      cp_async8(dst + 16 * kGuPitch + lane * 8, s13 + grow * kHBlocks + bb);
+    if (lane < 16 && (lane & 7) < U.nr) {              // 16 rows x kGuU scale bytes
+      const size_t grow = (size_t)(lane < 8 ? U.j0 + lane : kI + U.j0 + (lane & 7));
+      cp_async8(dst + 16 * pitch + lane * 8, U.s13 + grow * kHBlocks + bb);
     }
   };
 #pragma unroll
-  for (int st = 0; st < kGuStages - 1; ++st) {
-    if (st < nst) issue(st);
+  for (int st = 0; st < STAGES - 1; ++st) {
+    if (st < total) issue(st);
     cp_async_commit();
   }
-  for (int st = 0; st < nst; ++st) {
-    if (st + kGuStages - 1 < nst) issue(st + kGuStages - 1);
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // even / odd blocks
+  float bcacc[2] = {0.f, 0.f};                                       // block columns: rows g, g + 8
+  for (int st = 0; st < total; ++st) {
+    if (st + STAGES - 1 < total) issue(st + STAGES - 1);
     cp_async_commit();
-    cp_async_wait<kGuStages - 1>();
+    cp_async_wait<STAGES - 1>();
     __syncwarp();
-    const uint8_t* buf = ring + (st % kGuStages) * kGuStageBytes;
-    const int bb = kb0 + st * kGuU;
+    if (st / spu != jc) { jc = st / spu; Uc = (jc == ji) ? Ui : info(jc); }
+    const GuUnit& U = Uc;
+    const bool rv = g < U.nr;
+    const uint8_t* buf = ring + (st % STAGES) * SBYTES;
+    const int bb = U.kb0 + (st % spu) * kGuU;
+    if (BC) {
+      constexpr int pitch = kGuU * 16;
+      const uint8_t* scp = buf + 16 * pitch;
+#pragma unroll
+      for (int sb = 0; sb < kGuU; sb += 4) {
+        const int pos = (sb + q) ^ ((g & 1) << 2);
+        uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+        uint32_t s0 = 0x7F7Fu, s1 = 0x7F7Fu;             // 1.0 for absent rows
+        if (rv) {
+          w0 = *reinterpret_cast<const uint4*>(buf + g * pitch + pos * 16);
+          w1 = *reinterpret_cast<const uint4*>(buf + (g + 8) * pitch + pos * 16);
+          s0 = *reinterpret_cast<const uint16_t*>(scp + g * 8 + sb + 2 * (q & 1));
+          s1 = *reinterpret_cast<const uint16_t*>(scp + (g + 8) * 8 + sb + 2 * (q & 1));
+        }
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        bc_step(w0, w1, U.xtok ? U.xtok + 64 * (bb + sb + q) : nullptr, d);
+        bc_scale_add(d, s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc);
+      }
+      __syncwarp();
+      if (st % spu == spu - 1) {
+        float r[4];
+        bc_finish(bcacc, q, r);
+        done(st / spu, r);
+        bcacc[0] = bcacc[1] = 0.f;
+      }
+      continue;
+    }
     uint2 scg = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu), scu = scg;
     if (rv) {
       scg = *reinterpret_cast<const uint2*>(buf + 16 * kGuPitch + g * 8);
       scu = *reinterpret_cast<const uint2*>(buf + 16 * kGuPitch + (g + 8) * 8);
     }
+    // fast path (every scale of the stage in the f16-exact range): the scale is folded into
+    // the f16 weights (an exact power-of-two multiply) and the MMAs accumulate directly
+    const bool fast = __all_sync(0xffffffffu, e8m0x4_f16_exact(scg.x) && e8m0x4_f16_exact(scg.y) &&
+                                                  e8m0x4_f16_exact(scu.x) && e8m0x4_f16_exact(scu.y));
 #pragma unroll
     for (int u = 0; u < kGuU; ++u) {
       uint32_t wg = 0, wu = 0;
@@ -529,37 +690,70 @@ __device__ __forceinline__ void gate_up_tile(const uint8_t* q13, const uint8_t* 
         wu = *reinterpret_cast<const uint32_t*>(buf + (g + 8) * kGuPitch + u * 16 + 4 * q);
       }
       uint4 xv = make_uint4(0, 0, 0, 0);
-      if (xtok) xv = *reinterpret_cast<const uint4*>(xtok + 64 * (bb + u) + 16 * q);
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(d, e2m1x2_to_f16x2(wg & 0xFF), e2m1x2_to_f16x2(wu & 0xFF),
-                e2m1x2_to_f16x2((wg >> 8) & 0xFF), e2m1x2_to_f16x2((wu >> 8) & 0xFF), xv.x, xv.y);
-      mma_16816(d, e2m1x2_to_f16x2((wg >> 16) & 0xFF), e2m1x2_to_f16x2((wu >> 16) & 0xFF),
-                e2m1x2_to_f16x2(wg >> 24), e2m1x2_to_f16x2(wu >> 24), xv.z, xv.w);
-      const uint32_t sgw = u < 4 ? scg.x : scg.y, suw = u < 4 ? scu.x : scu.y;
-      const float fg = e8m0_to_f32((sgw >> (8 * (u & 3))) & 0xFF);
-      const float fu = e8m0_to_f32((suw >> (8 * (u & 3))) & 0xFF);
-      acc[0] = fmaf(fg, d[0], acc[0]);
-      acc[1] = fmaf(fg, d[1], acc[1]);
-      acc[2] = fmaf(fu, d[2], acc[2]);
-      acc[3] = fmaf(fu, d[3], acc[3]);
+      if (U.xtok) xv = *reinterpret_cast<const uint4*>(U.xtok + 64 * (bb + u) + 16 * q);
+      const uint32_t sgb = ((u < 4 ? scg.x : scg.y) >> (8 * (u & 3))) & 0xFF;
+      const uint32_t sub = ((u < 4 ? scu.x : scu.y) >> (8 * (u & 3))) & 0xFF;
+      uint32_t hg[4], hu[4];
+      e2m1x8_to_f16x2x4(wg, hg);
+      e2m1x8_to_f16x2x4(wu, hu);
+      if (fast) {
+        const uint32_t fg = e8m0_to_f16x2_pow2(sgb), fu = e8m0_to_f16x2_pow2(sub);
+        float (&a)[4] = acc[u & 1];
+        mma_16816(a, hmul2_u32(hg[0], fg), hmul2_u32(hu[0], fu), hmul2_u32(hg[1], fg), hmul2_u32(hu[1], fu), xv.x, xv.y);
+        mma_16816(a, hmul2_u32(hg[2], fg), hmul2_u32(hu[2], fu), hmul2_u32(hg[3], fg), hmul2_u32(hu[3], fu), xv.z, xv.w);
+      } else {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(d, hg[0], hu[0], hg[1], hu[1], xv.x, xv.y);
+        mma_16816(d, hg[2], hu[2], hg[3], hu[3], xv.z, xv.w);
+        const float fg = e8m0_to_f32(sgb), fu = e8m0_to_f32(sub);
+        float (&a)[4] = acc[u & 1];
+        a[0] = fmaf(fg, d[0], a[0]);
+        a[1] = fmaf(fg, d[1], a[1]);
+        a[2] = fmaf(fu, d[2], a[2]);
+        a[3] = fmaf(fu, d[3], a[3]);
+      }
     }
     __syncwarp();
+    if (st % spu == spu - 1) {
+      const float r[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]};
+      done(st / spu, r);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
+    }
   }
 }
 
 // Tile list of virtual row pairs [a, b) (slot s covers [s*kI, (s+1)*kI), slot_offset added):
 // tiles of up to 8 row pairs inside one slot, one entry per 8-token column group.
-__device__ void build_gate_up_tiles(const Tables& tb, int a, int b, int slot_offset, Tables& out) {
+__device__ void build_gate_up_tiles(Tables& tb, int a, int b) {
+  // thread 0 lays out the few slot segments the range touches; then every thread writes
+  // entries (segment-major, then tile, then column group)
   if (threadIdx.x == 0) {
-    int n = 0;
-    while (a < b && n < kGuMaxTiles) {
-      const int slot = a / kI + slot_offset, j0 = a % kI;
-      const int nr = min(8, min(kI - j0, b - a));
+    int n = 0, k = 0;
+    while (a < b && k < kMaxSegs) {
+      const int slot = a / kI, ja = a % kI, jb = min(kI, ja + (b - a));
       const int m = tb.slot_begin[slot + 1] - tb.slot_begin[slot];
-      for (int n0 = 0; n0 < m && n < kGuMaxTiles; n0 += 8) out.gu_tile[n++] = make_int4(slot, j0, nr, n0);
-      a += nr;
+      tb.seg_slot[k] = slot;
+      tb.seg_lo[k] = ja;
+      tb.seg_hi[k] = jb;
+      tb.seg_groups[k] = (m + 7) / 8;
+      tb.seg_off[k] = n;
+      n += (jb - ja + 7) / 8 * tb.seg_groups[k];
+      a += jb - ja;
+      ++k;
     }
-    out.gu_n = n;
+    tb.n_segs = k;
+    tb.seg_off[k] = n;
+    tb.gu_n = (a < b || n > kGuMaxTiles) ? -1 : n;      // -1: the block's share does not fit
+  }
+  __syncthreads();
+  const int n = tb.gu_n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    int k = 0;
+    while (i >= tb.seg_off[k + 1]) ++k;
+    const int r = i - tb.seg_off[k], gq = tb.seg_groups[k];
+    const int j0 = tb.seg_lo[k] + 8 * (r / gq);
+    tb.gu_tile[i] = make_int4(tb.seg_slot[k], j0, min(8, tb.seg_hi[k] - j0), 8 * (r % gq));
   }
   __syncthreads();
 }
@@ -567,50 +761,53 @@ __device__ void build_gate_up_tiles(const Tables& tb, int a, int b, int slot_off
 // All gate/up tiles of the block's list: units (tile, K half) in rounds of kGuRound; the two
 // halves' partials are summed in a fixed order, then SwiGLU, then h per (pair, row).
 __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, Tables& tb,
-                              bool prefetch) {
+                              int trace_layer = kTraceNone) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   float4* red = reinterpret_cast<float4*>(const_cast<uint8_t*>(smem) + smem_layout(p.M).gured);
-  // K split per tile (a divisor of the 10 stages of 8 blocks): about one unit per warp when
-  // the block has few tiles, whole tiles (10 pipelined stages) when it has many
-  const int want = kWarps / max(1, tb.gu_n);
-  const int ks = want >= 10 ? 10 : want >= 5 ? 5 : want >= 2 ? 2 : 1;
+  // K split per tile: ks parts of 10 / ks stages (8 blocks each), chosen to minimise the
+  // stages of the busiest warp, ceil(tiles * ks / warps) * 10 / ks (ties: the smaller ks)
+  int ks = 1, best = 1 << 30;
+  for (int c = 1; c <= 10; ++c) {
+    if (10 % c != 0) continue;
+    const int cost = (tb.gu_n * c + kWarps - 1) / kWarps * (10 / c);
+    if (cost < best) { best = cost; ks = c; }
+  }
   const int units = tb.gu_n * ks;
   const int kpart = kHBlocks / ks;
+  const bool bc = p.M <= 2;                        // block-column MMAs (at most two tokens a tile)
   const int round = kGuRound / ks * ks;            // a whole number of tiles per round
+  uint8_t* ring = const_cast<uint8_t*>(smem) + smem_layout(p.M).ring + (size_t)warp * warp_ring_bytes(p.M);
   for (int u0 = 0; u0 < units; u0 += round) {
     const int un = min(round, units - u0);
-    // each warp's lane 0 first asks L2 for its own units' rows (bulk prefetches of the
-    // tile's 8 contiguous gate rows and 8 contiguous up rows, and their scales)
-    if (lane == 0 && prefetch) {
-      for (int u = warp; u < un; u += kWarps) {
-        const int4 t = tb.gu_tile[(u0 + u) / ks];
-        const int kp = (u0 + u) % ks;
-        const int e = tb.slot_expert[t.x];
-        const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
-        const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
-        if (kp == 0) {                   // the tile's first K part prefetches the whole tile
-          prefetch_l2(q13 + (size_t)t.y * kW13RowBytes, t.z * kW13RowBytes);
-          prefetch_l2(q13 + (size_t)(kI + t.y) * kW13RowBytes, t.z * kW13RowBytes);
-          prefetch_l2(s13 + (size_t)t.y * kHBlocks, t.z * kHBlocks);
-          prefetch_l2(s13 + (size_t)(kI + t.y) * kHBlocks, t.z * kHBlocks);
-        }
-      }
-    }
-    for (int u = warp; u < un; u += kWarps) {
-      const int4 t = tb.gu_tile[(u0 + u) / ks];
-      const int kp = (u0 + u) % ks;
-      const int slot = t.x, e = tb.slot_expert[slot];
-      const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
-      const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
+    MDW_TRACE_POINT(trace_layer, 15);
+    const int mine = un > warp ? (un - warp + kWarps - 1) / kWarps : 0;
+    auto info = [&](int j) {
+      const int u = u0 + warp + j * kWarps;
+      const int4 t = tb.gu_tile[u / ks];
+      const int kp = u % ks, slot = t.x, e = tb.slot_expert[slot];
       const int pb = tb.slot_begin[slot], m = tb.slot_begin[slot + 1] - pb;
-      const uint8_t* xtok = (t.w + g < m) ? smem + (size_t)tb.pair_token[pb + t.w + g] * kXhBytes : nullptr;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      uint8_t* ring = const_cast<uint8_t*>(smem) + smem_layout(p.M).ring + (size_t)warp * kWarpRing;
-      gate_up_tile(q13, s13, t.y, t.z, xtok, kp * kpart, (kp + 1) * kpart, acc, ring, lane);
-      red[u * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    }
+      GuUnit U;
+      U.q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
+      U.s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
+      if (bc) {       // lane (g, q) feeds token g >> 2 of the tile, on its own block q == g & 3
+        const int tt = g >> 2;
+        U.xtok = (q == (g & 3) && t.w + tt < m) ? smem + (size_t)tb.pair_token[pb + t.w + tt] * kXhBytes : nullptr;
+      } else {
+        U.xtok = (t.w + g < m) ? smem + (size_t)tb.pair_token[pb + t.w + g] * kXhBytes : nullptr;
+      }
+      U.j0 = t.y;
+      U.nr = t.z;
+      U.kb0 = kp * kpart;
+      return U;
+    };
+    auto done = [&](int j, const float (&acc)[4]) {
+      red[(warp + j * kWarps) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    };
+    if (bc) gate_up_units<true>(mine, 10 / ks, info, done, ring, lane);
+    else gate_up_units<false>(mine, 10 / ks, info, done, ring, lane);
     __syncthreads();
+    MDW_TRACE_POINT(trace_layer, 16);
     for (int u = warp; u < un; u += kWarps) {
       if ((u0 + u) % ks != 0) continue;
       const int4 t = tb.gu_tile[(u0 + u) / ks];
@@ -686,7 +883,7 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
   float* part = reinterpret_cast<float*>(smem + sl.part);
   float* yacc = reinterpret_cast<float*>(smem + sl.yacc);
   float4* red = reinterpret_cast<float4*>(smem + sl.gured);
-  uint8_t* ring = smem + sl.ring + (size_t)warp * kWarpRing;
+  uint8_t* ring = smem + sl.ring + (size_t)warp * warp_ring_bytes(M);
   for (int i = threadIdx.x; i < M * kMaxRowsPerBlock; i += blockDim.x) yacc[i] = 0.f;
   auto w2_of = [&](int slot, const uint8_t*& q2, const uint8_t*& s2) {
     const int e = tb.slot_expert[slot];
@@ -694,24 +891,62 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
   };
   const int NP = tb.n_pairs;
+  const bool bc = M <= 2;                          // block-column MMAs (at most two pairs a slot)
   for (int q0 = 0; q0 < NP; q0 += kPairChunk) {
     const int n = min(kPairChunk, NP - q0);
     __syncthreads();
+    MDW_TRACE_POINT(layer, 17);
     quantise_pairs(p, smem, tb, q0, n);
+    MDW_TRACE_POINT(layer, 18);
     // unit list: (slot, full tile, K half, 8-token group)
-    if (threadIdx.x == 0) {
-      int cnt = 0;
+    // the slots of the chunk (at most kPairChunk + 1 <= 32: one per lane of warp 0) and their
+    // unit counts (tiles x 8-pair groups x 2 K halves), scanned; then every thread writes units
+    if (warp == 0) {
       const int s_lo = tb.pair_slot[q0], s_hi = tb.pair_slot[q0 + n - 1];
-      for (int sidx = s_lo; sidx <= s_hi; ++sidx) {
-        const int pa = max(tb.slot_begin[sidx], q0), pz = min(tb.slot_begin[sidx + 1], q0 + n);
-        for (int tile = 0; tile < nfull; ++tile)
-          for (int ng = pa; ng < pz; ng += 8)
-            for (int kp = 0; kp < 2 && cnt < kGuMaxTiles; ++kp) tb.gu_tile[cnt++] = make_int4(sidx, tile, kp, ng);
+      const int sidx = s_lo + lane;
+      int c = 0, pa = 0;
+      if (sidx <= s_hi) {
+        pa = max(tb.slot_begin[sidx], q0);
+        const int pz = min(tb.slot_begin[sidx + 1], q0 + n);
+        c = nfull * ((pz - pa + 7) / 8) * 2;
       }
-      tb.gu_n = cnt;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      if (sidx <= s_hi) {
+        tb.seg_slot[lane] = sidx;
+        tb.seg_lo[lane] = pa;
+        tb.seg_groups[lane] = c / (2 * max(1, nfull));
+        tb.seg_off[lane] = incl - c;
+      }
+      if (lane == 0) tb.n_segs = s_hi - s_lo + 1;
+      if (sidx == s_hi) { tb.seg_off[lane + 1] = incl; tb.gu_n = incl; }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < tb.gu_n; i += blockDim.x) {
+      int k = 0;
+      while (i >= tb.seg_off[k + 1]) ++k;
+      const int r = i - tb.seg_off[k], gq = tb.seg_groups[k];
+      const int kp = r & 1, tg = r >> 1;
+      tb.gu_tile[i] = make_int4(tb.seg_slot[k], tg / gq, kp, tb.seg_lo[k] + 8 * (tg % gq));
     }
     __syncthreads();
     MDW_TRACE_POINT(layer, 13);
+    // leftover rows (nrows mod 16, CUDA cores, one warp per (pair, row)): the weights of
+    // this warp's first item are requested now, so they arrive while the tiles run
+    const int rem_items = n * nrem;
+    uint4 rem_w = make_uint4(0, 0, 0, 0);
+    uint32_t rem_s = 0;
+    if (warp < rem_items && lane < kIBlocks) {
+      const int k2 = warp / nrem, rr = 16 * nfull + warp % nrem;
+      const uint8_t *q2, *s2;
+      w2_of(tb.pair_slot[q0 + k2], q2, s2);
+      rem_w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
+      rem_s = ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane);
+    }
     const int units = tb.gu_n;
     for (int u0 = 0; u0 < units; u0 += kGuRound) {
       const int un = min(kGuRound, units - u0);
@@ -722,16 +957,17 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
         w2_of(t.x, q2, s2);
         uint8_t* dst = ring + (k % kDnStages) * kDnStageBytes;
         const int rb = r0 + 16 * t.y, kb0 = t.z * kDnKB;
+        const int pitch = bc ? kDnBcPitch : kDnPitch;
 #pragma unroll
         for (int j = 0; j < 16 * kDnKB / 32; ++j) {     // 16 rows x 12 chunks of 16 bytes
           const int c = lane + 32 * j, row = c / kDnKB, blk = c % kDnKB;
-          cp_async16(dst + row * kDnPitch + blk * 16, q2 + (size_t)(rb + row) * kW2RowBytes + (kb0 + blk) * 16);
+          cp_async16(dst + row * pitch + blk * 16, q2 + (size_t)(rb + row) * kW2RowBytes + (kb0 + blk) * 16);
         }
         if (lane < 16 * 3 / 2) {                         // 16 rows x 24 scale bytes, 8 at a time
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int c = lane + 24 * j, row = c / 3, part8 = c % 3;
-            cp_async8(dst + 16 * kDnPitch + row * kIBlocks + part8 * 8,
+            cp_async8(dst + 16 * pitch + row * kIBlocks + part8 * 8,
                       s2 + (size_t)(rb + row) * kIBlocks + part8 * 8);
           }
         }
@@ -747,32 +983,76 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
         const int4 t = tb.gu_tile[u0 + warp + k * kWarps];
         const int pz = min(tb.slot_begin[t.x + 1], q0 + n);
         const int kb0 = t.z * kDnKB;
+        if (bc) {
+          // block columns: lane (g, q) feeds pair t.w + (g >> 2) on its own block q == g & 3
+          const int tt = g >> 2;
+          const uint8_t* hbc = (qd == (g & 3) && t.w + tt < pz) ? smem + sl.hh + (size_t)(t.w + tt - q0) * kHhBytes : nullptr;
+          const uint8_t* scp = buf + 16 * kDnBcPitch;
+          float bcacc[2] = {0.f, 0.f};
+#pragma unroll
+          for (int sb = 0; sb < kDnKB; sb += 4) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(buf + g * kDnBcPitch + (sb + qd) * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(buf + (g + 8) * kDnBcPitch + (sb + qd) * 16);
+            const uint32_t s0 = *reinterpret_cast<const uint16_t*>(scp + g * kIBlocks + kb0 + sb + 2 * (qd & 1));
+            const uint32_t s1 = *reinterpret_cast<const uint16_t*>(scp + (g + 8) * kIBlocks + kb0 + sb + 2 * (qd & 1));
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            bc_step(w0, w1, hbc ? hbc + 64 * (kb0 + sb + qd) : nullptr, d);
+            bc_scale_add(d, s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc);
+          }
+          float r[4];
+          bc_finish(bcacc, qd, r);
+          __syncwarp();
+          red[(warp + k * kWarps) * 32 + lane] = make_float4(r[0], r[1], r[2], r[3]);
+          continue;
+        }
         // B column g = token pair t.w + g of the slot (if it exists in this chunk)
         const uint8_t* hb = (t.w + g < pz) ? smem + sl.hh + (size_t)(t.w + g - q0) * kHhBytes : nullptr;
         const uint8_t* sc_g = buf + 16 * kDnPitch + g * kIBlocks + kb0;
         const uint8_t* sc_g8 = buf + 16 * kDnPitch + (g + 8) * kIBlocks + kb0;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+        // scales of the unit (12 blocks of rows g and g + 8): fast path as in the gate/up units
+        uint32_t sa3[3], sb3[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          sa3[i] = reinterpret_cast<const uint32_t*>(sc_g)[i];      // 4-byte aligned: 3328 + 24 g + 12 kp
+          sb3[i] = reinterpret_cast<const uint32_t*>(sc_g8)[i];
+        }
+        const bool fast = __all_sync(0xffffffffu, e8m0x4_f16_exact(sa3[0]) && e8m0x4_f16_exact(sa3[1]) &&
+                                                      e8m0x4_f16_exact(sa3[2]) && e8m0x4_f16_exact(sb3[0]) &&
+                                                      e8m0x4_f16_exact(sb3[1]) && e8m0x4_f16_exact(sb3[2]));
+        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
         for (int b = 0; b < kDnKB; ++b) {
           const uint32_t wa = *reinterpret_cast<const uint32_t*>(buf + g * kDnPitch + b * 16 + 4 * qd);
           const uint32_t wb = *reinterpret_cast<const uint32_t*>(buf + (g + 8) * kDnPitch + b * 16 + 4 * qd);
           uint4 xv = make_uint4(0, 0, 0, 0);
           if (hb) xv = *reinterpret_cast<const uint4*>(hb + 64 * (kb0 + b) + 16 * qd);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_16816(d, e2m1x2_to_f16x2(wa & 0xFF), e2m1x2_to_f16x2(wb & 0xFF),
-                    e2m1x2_to_f16x2((wa >> 8) & 0xFF), e2m1x2_to_f16x2((wb >> 8) & 0xFF), xv.x, xv.y);
-          mma_16816(d, e2m1x2_to_f16x2((wa >> 16) & 0xFF), e2m1x2_to_f16x2((wb >> 16) & 0xFF),
-                    e2m1x2_to_f16x2(wa >> 24), e2m1x2_to_f16x2(wb >> 24), xv.z, xv.w);
-          const float fa = e8m0_to_f32(sc_g[b]), fb = e8m0_to_f32(sc_g8[b]);
-          acc[0] = fmaf(fa, d[0], acc[0]);
-          acc[1] = fmaf(fa, d[1], acc[1]);
-          acc[2] = fmaf(fb, d[2], acc[2]);
-          acc[3] = fmaf(fb, d[3], acc[3]);
+          uint32_t ha[4], hc[4];
+          e2m1x8_to_f16x2x4(wa, ha);
+          e2m1x8_to_f16x2x4(wb, hc);
+          const uint32_t sab = (sa3[b >> 2] >> (8 * (b & 3))) & 0xFF, sbb = (sb3[b >> 2] >> (8 * (b & 3))) & 0xFF;
+          float (&a)[4] = acc2[b & 1];
+          if (fast) {
+            const uint32_t fa = e8m0_to_f16x2_pow2(sab), fb = e8m0_to_f16x2_pow2(sbb);
+            mma_16816(a, hmul2_u32(ha[0], fa), hmul2_u32(hc[0], fb), hmul2_u32(ha[1], fa), hmul2_u32(hc[1], fb), xv.x, xv.y);
+            mma_16816(a, hmul2_u32(ha[2], fa), hmul2_u32(hc[2], fb), hmul2_u32(ha[3], fa), hmul2_u32(hc[3], fb), xv.z, xv.w);
+          } else {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(d, ha[0], hc[0], ha[1], hc[1], xv.x, xv.y);
+            mma_16816(d, ha[2], hc[2], ha[3], hc[3], xv.z, xv.w);
+            const float fa = e8m0_to_f32(sab), fb = e8m0_to_f32(sbb);
+            a[0] = fmaf(fa, d[0], a[0]);
+            a[1] = fmaf(fa, d[1], a[1]);
+            a[2] = fmaf(fb, d[2], a[2]);
+            a[3] = fmaf(fb, d[3], a[3]);
+          }
         }
+        const float acc[4] = {acc2[0][0] + acc2[1][0], acc2[0][1] + acc2[1][1], acc2[0][2] + acc2[1][2],
+                              acc2[0][3] + acc2[1][3]};
         __syncwarp();
         red[(warp + k * kWarps) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       }
       __syncthreads();
+      MDW_TRACE_POINT(layer, 19);
       // K halves added in order (unit kp = 0 owns the pair); D rows = W2 rows g, g + 8;
       // D columns 2qd, 2qd + 1 = pairs t.w + 2qd (+1)
       for (int u = warp; u < un; u += kWarps) {
@@ -792,16 +1072,17 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
         }
       }
     }
-    // leftover rows: one warp per (pair, row); lanes 0..23 one block each
-    const int rem_items = n * nrem;
+    // leftover rows: lanes 0..23 one block each
     for (int it = warp; it < rem_items; it += kWarps) {
       const int k2 = it / nrem, rr = 16 * nfull + it % nrem, q = q0 + k2;
-      const uint8_t *q2, *s2;
-      w2_of(tb.pair_slot[q], q2, s2);
       float dsum = 0.f;
       if (lane < kIBlocks) {
-        const uint4 w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
-        const float sc = e8m0_to_f32(ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane));
+        if (it != warp) {
+          const uint8_t *q2, *s2;
+          w2_of(tb.pair_slot[q], q2, s2);
+          rem_w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
+          rem_s = ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane);
+        }
         const uint8_t* hh = smem + sl.hh + (size_t)k2 * kHhBytes + 64 * lane;
         uint32_t x2[16];
 #pragma unroll
@@ -809,7 +1090,7 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
           const uint4 xv = *reinterpret_cast<const uint4*>(hh + 16 * pl);
           x2[4 * pl] = xv.x; x2[4 * pl + 1] = xv.y; x2[4 * pl + 2] = xv.z; x2[4 * pl + 3] = xv.w;
         }
-        dsum = mx_block_dot(w, x2) * sc;
+        dsum = mx_block_dot(rem_w, x2) * e8m0_to_f32(rem_s);
       }
       dsum = warp_sum(dsum);
       if (lane == 0) part[k2 * kMaxRowsPerBlock + rr] = dsum * tb.sh[k2] * tb.pair_gate[q];
@@ -843,44 +1124,60 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
   }
 }
 
-// L2 prefetch of [base, base + bytes), one 128-byte line per thread per step, spread over
-// all threads of the block (non-blocking: the instructions carry no destination register).
-__device__ __forceinline__ void prefetch_range(const void* base, size_t bytes) {
-  const char* b = static_cast<const char*>(base);
-  for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)blockDim.x * 128)
-    asm volatile("prefetch.global.L2 [%0];" :: "l"(b + off));
-  if (threadIdx.x == 0 && bytes > 0) asm volatile("prefetch.global.L2 [%0];" :: "l"(b + bytes - 1));
+// Bulk L2 prefetch of [base + lo, base + hi) shrunk to 16-byte boundaries (the TMA unit
+// handles it, so the SM's load path stays free).
+__device__ __forceinline__ void prefetch_bulk(const uint8_t* base, size_t lo, size_t hi) {
+  lo = (lo + 15) & ~(size_t)15;
+  hi &= ~(size_t)15;
+  if (hi > lo) prefetch_l2(base + lo, (uint32_t)(hi - lo));
 }
 
-// The block's W2 rows (and scales) of every slot: lane 0 of warp (slot mod warps) issues
-// the two bulk L2 prefetches of a slot (rows r0..r1 of W2 are contiguous).
-__device__ void prefetch_down(const MoeParams& p, const LayerDesc& L, const Tables& tb) {
+// L2 prefetch of every weight byte the block reads in the layer, as soon as the slots are
+// known: its gate/up row pairs [a, b) of the slot space (gate rows, up rows, their scales)
+// first, then its W2 rows [r0, r1) (and scales) of every slot. The contiguous ranges are
+// dealt to lane 0 of warps 1, 2, ... (warp 0 is building the routing tables meanwhile).
+__device__ void prefetch_block_weights(const MoeParams& p, const LayerDesc& L, const Tables& tb, int a, int b) {
   const int G = gridDim.x;
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) != 0 || warp == 0) return;
+  int k = 0;
+  auto mine = [&]() { return 1 + k++ % (kWarps - 1) == warp; };
+  while (a < b) {
+    const int slot = a / kI, ja = a % kI, jb = min(kI, ja + (b - a));
+    const int e = tb.slot_expert[slot];
+    const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
+    const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
+    for (int half = 0; half < 2; ++half) {
+      const size_t row = (size_t)half * kI;
+      if (mine()) prefetch_bulk(q13, (row + ja) * kW13RowBytes, (row + jb) * kW13RowBytes);
+      if (mine()) prefetch_bulk(s13, (row + ja) * kHBlocks, (row + jb) * kHBlocks);
+    }
+    a += jb - ja;
+  }
   const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
-  if ((threadIdx.x & 31) != 0) return;
-  for (int s = threadIdx.x >> 5; s < tb.n_slots; s += kWarps) {
+  for (int s = 0; s < tb.n_slots; ++s) {
     const int e = tb.slot_expert[s];
     const uint8_t* q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
     const uint8_t* s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
-    prefetch_l2(q2 + (size_t)r0 * kW2RowBytes, (uint32_t)((r1 - r0) * kW2RowBytes));
-    const size_t sb = ((size_t)r0 * kIBlocks) & ~(size_t)15;
-    const size_t se = ((size_t)r1 * kIBlocks + 15) & ~(size_t)15;
-    prefetch_l2(s2 + sb, (uint32_t)(se - sb));
+    if (mine()) prefetch_bulk(q2, (size_t)r0 * kW2RowBytes, (size_t)r1 * kW2RowBytes);
+    if (mine()) prefetch_bulk(s2, (size_t)r0 * kIBlocks, (size_t)r1 * kIBlocks);
   }
 }
 
-// This block's router rows and shared-expert slice of a layer (routing-independent).
+// This block's router rows and shared-expert slice of a layer (routing-independent): five
+// bulk L2 prefetches, from lane 0 of warps 0..4.
 __device__ void prefetch_static(const MoeParams& p, const LayerDesc& L) {
   const int G = gridDim.x, E = p.E;
-  const int e0 = (int)((long long)blockIdx.x * E / G), e1 = (int)((long long)(blockIdx.x + 1) * E / G);
-  prefetch_range(L.router_w + (size_t)e0 * kH, (size_t)(e1 - e0) * kH * 2);
-  if (p.has_shared) {
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) != 0 || warp > 4) return;
+  if (warp == 0) {
+    const int e0 = (int)((long long)blockIdx.x * E / G), e1 = (int)((long long)(blockIdx.x + 1) * E / G);
+    prefetch_l2(L.router_w + (size_t)e0 * kH, (uint32_t)((e1 - e0) * kH * 2));
+  } else if (p.has_shared) {
     const int j0 = (int)((long long)blockIdx.x * kI / G), j1 = (int)((long long)(blockIdx.x + 1) * kI / G);
-    for (int half = 0; half < 2; ++half) {
-      const size_t row = (size_t)half * kI + j0;
-      prefetch_range(L.sh_w13_q + row * kW13RowBytes, (size_t)(j1 - j0) * kW13RowBytes);
-      prefetch_range(L.sh_w13_s + row * kHBlocks, (size_t)(j1 - j0) * kHBlocks);
-    }
+    const size_t row = (size_t)((warp - 1) & 1) * kI + j0;
+    if (warp <= 2) prefetch_l2(L.sh_w13_q + row * kW13RowBytes, (uint32_t)((j1 - j0) * kW13RowBytes));
+    else prefetch_l2(L.sh_w13_s + row * kHBlocks, (uint32_t)((j1 - j0) * kHBlocks));
   }
 }
 
@@ -895,35 +1192,34 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
   for (int layer = 0; layer < p.L; ++layer) {
     const LayerDesc& L = p.layers[layer];
     MDW_TRACE_POINT(layer, 0);
-    prepare_input<MAXM>(p, layer, smem, tb);
-    MDW_TRACE_POINT(layer, 1);
-    router_rows(p, L, smem);
+    {
+      // the router row's weights are requested before the input, so the two loads overlap
+      uint4 wv[10];
+      int e0, e1;
+      router_range(p, e0, e1);
+      if (e0 + (int)(threadIdx.x >> 5) < e1) load_router_row(L, e0 + (threadIdx.x >> 5), wv);
+      prepare_input<MAXM>(p, layer, smem, tb);
+      MDW_TRACE_POINT(layer, 1);
+      router_rows(p, L, smem, wv);
+    }
     bar.arrive();                                                   // B1 (logits)
     MDW_TRACE_POINT(layer, 2);
-    if (p.has_shared) {
-      // shared expert: static slice of its row pairs, needs only x-hat
-      if (threadIdx.x == 0) { tb.slot_expert[0] = -1; tb.slot_begin[0] = 0; tb.slot_begin[1] = p.M; }
-      if (threadIdx.x < p.M) tb.pair_token[threadIdx.x] = threadIdx.x;
-      __syncthreads();
-      const int j0 = (int)((long long)blockIdx.x * kI / G), j1 = (int)((long long)(blockIdx.x + 1) * kI / G);
-      build_gate_up_tiles(tb, j0, j1, 0, tb);
-      gate_up_tiles(p, L, smem, tb, false);
-    }
     MDW_TRACE_POINT(layer, 3);
     if (!bar.wait()) return;
     MDW_TRACE_POINT(layer, 4);
-    route_tokens(p, tb, layer, smem + smem_layout(p.M).gured);
+    route_tokens(p, L, tb, layer, smem + smem_layout(p.M).gured);
     __syncthreads();
     if (tb.bad) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
     {
-      const int first = p.has_shared ? 1 : 0;
-      const long long PR = (long long)tb.n_routed * kI;
+      // gate/up row pairs of every slot (the shared expert is slot 0), dealt to the blocks
+      // in equal contiguous shares
+      const long long PR = (long long)tb.n_slots * kI;
       const int a = (int)((long long)blockIdx.x * PR / G), b = (int)((long long)(blockIdx.x + 1) * PR / G);
       MDW_TRACE_POINT(layer, 12);
-      prefetch_down(p, L, tb);
       MDW_TRACE_POINT(layer, 5);
-      build_gate_up_tiles(tb, a, b, first, tb);
-      gate_up_tiles(p, L, smem, tb, true);
+      build_gate_up_tiles(tb, a, b);
+      if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
+      gate_up_tiles(p, L, smem, tb, layer);
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);

@@ -218,3 +218,50 @@ def test_device_weights_match_host_regeneration(layer512):
             assert np.array_equal(dev.cpu().numpy(), hst)
     for dev, hst in zip(sh, layer512.shared()):
         assert np.array_equal(dev.cpu().numpy(), hst)
+
+
+def _widen_scales(s: torch.Tensor) -> torch.Tensor:
+    """Move two thirds of the rows' E8M0 scales outside [113, 140] (the range in which the
+    kernels fold the scale into their f16 weights): rows with row % 3 == 0 get 105..112
+    (2^-22 .. 2^-15), row % 3 == 1 get 141..145 (2^14 .. 2^18), the rest keep theirs. A row
+    stays within one regime, so its dot products keep an fp32-friendly dynamic range (gate
+    row j and up row 768 + j share a regime). Works on [.., rows, blocks] tensors."""
+    rows, blocks = s.shape[-2], s.shape[-1]
+    r = torch.arange(rows, device=s.device).view(rows, 1)
+    b = torch.arange(blocks, device=s.device).view(1, blocks)
+    k = (r % 3).expand(rows, blocks)
+    lo = (105 + (r + b) % 8).to(torch.uint8)
+    hi = (141 + (r + b) % 5).to(torch.uint8)
+    return torch.where(k == 0, lo, torch.where(k == 1, hi, s))
+
+
+class WideScaleLayer(Layer):
+    """A layer whose E8M0 scales leave the f16-exact range: the kernels must take their
+    fp32-scaling path for those blocks and still match the oracle."""
+
+    def __init__(self):
+        super().__init__(seed=11, layer=2, num_experts=64, top_k=8, shared=True)
+        wr, w13q, w13s, w2q, w2s, sh = self.tensors
+        w13s.copy_(_widen_scales(w13s))
+        w2s.copy_(_widen_scales(w2s))
+        sh[1].copy_(_widen_scales(sh[1]))
+        sh[3].copy_(_widen_scales(sh[3]))
+
+    def expert(self, e: int):
+        if e not in self._cache:
+            q13, s13, q2, s2 = synth.expert_tensors(self.seed, self.layer, e)
+            self._cache[e] = (q13.numpy(), _widen_scales(s13).numpy(), q2.numpy(), _widen_scales(s2).numpy())
+        return self._cache[e]
+
+
+def test_scales_outside_f16_exact_range():
+    layer = WideScaleLayer()
+    _, w13q, w13s, w2q, w2s, sh = layer.tensors
+    host = layer.expert(5)
+    assert np.array_equal(w13s[5].cpu().numpy(), host[1]) and np.array_equal(w2s[5].cpu().numpy(), host[3])
+    assert (host[1] < 113).any() and (host[1] > 140).any()
+    for m in (1, 4):
+        x = hidden_with_gap(60 + m, m, layer.wr, layer.K)
+        out = run_layer(layer, x)
+        y_tf = check_layer(layer, x, out)
+        assert_bar(out["y"].cpu().numpy(), y_tf, f"y (scales outside the f16-exact range, M={m})")
