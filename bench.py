@@ -130,9 +130,10 @@ def build_model(device, L: int, seed: int = 3):
 class Stepper:
     """Buffers and the two C-ABI calls of one decode step for M tokens."""
 
-    def __init__(self, layers, head, m: int, device, pool: int = 8):
+    def __init__(self, layers, head, m: int, device, pool: int = 8, override=None):
         from moe_decode_weight_gb300 import api, synth
         self.api, self.m, self.L = api, m, len(layers)
+        self.override = override              # int32 [L, M, K] imposed routing, or None
         self.layers = layers
         self.arr = api._layer_array(layers)
         self.head = head
@@ -146,7 +147,10 @@ class Stepper:
         self.topk = torch.zeros((m, TOPK_VOCAB), dtype=torch.int32, device=device)
 
     def layers_call(self, r0):
-        self.api.moe_decode_stack(self.arr, None, r0, None, self.ws, resid_out=self.resid)
+        if self.override is None:
+            self.api.moe_decode_stack(self.arr, None, r0, None, self.ws, resid_out=self.resid)
+        else:
+            self.api.moe_decode_stack_routed(self.arr, None, r0, None, self.ws, self.override, resid_out=self.resid)
 
     def head_call(self):
         self.api.lm_head_fp8_rmsnorm(self.head, self.resid[self.L], self.argmax, self.hws,
@@ -294,6 +298,83 @@ def _workload(m: int) -> str:
             f"bf16 pre-norm residual) + online-FP8 LM head 157184x2560 + argmax/top-29, M={m}")
 
 
+def sweep(layers, head, device, ms=(1, 2, 4, 8, 16), steps: int = 3, warmup: int = 3):
+    """The layer stack at several M, with the router's own routing and with Zipf(1.1)-popular
+    routing imposed (seed 4 + layer): per M the step time, the mean realised union and the
+    achieved GB/s of the stack (algorithmic bytes of the realised unions)."""
+    from moe_decode_weight_gb300 import synth
+    out = {}
+    for routing in ("uniform", "zipf"):
+        rows = []
+        for m in ms:
+            ov = None
+            if routing == "zipf":
+                ov = torch.from_numpy(np.stack([synth.zipf_topk(4 + l, m) for l in range(len(layers))])).to(device)
+            st = Stepper(layers, head, m, device, pool=2, override=ov)
+            r = time_steps(st, steps, warmup, lambda: None)
+            lay = float(np.mean(r["layer_ms"]))
+            rows.append({"M": m, "layer_stack_us": lay * 1000, "us_per_token": lay * 1000 / m,
+                         "mean_union": float(np.mean([np.mean(u) for u in r["unions"]])),
+                         "layer_stack_gbs": float(np.mean(r["bytes_layers"])) / (lay * 1e6)})
+            del st
+        out[routing] = rows
+    return out
+
+
+def fp8_vs_bf16(head, w_bf16, device, n: int = 64, k: int = TOPK_VOCAB):
+    """Agreement of the FP8 head with the BF16 head on n synthetic hidden states (seed 16):
+    top-1 agreement and the mean overlap of the two top-k sets."""
+    from moe_decode_weight_gb300 import api, synth
+    bf = api.mdw_lm_head_bf16_init(w_bf16)
+    m = 16
+    agree, overlap = 0, 0.0
+    for b in range(n // m):
+        x = _rmsnorm_bf16(synth.hidden_states(16, m, b).to(device))      # the same x for both heads
+        res = []
+        for fn, hd in ((api.lm_head_fp8, head), (api.lm_head_bf16, bf)):
+            ws = torch.zeros(api.mdw_lm_head_workspace_bytes(hd, m, k), dtype=torch.uint8, device=device)
+            am = torch.zeros(m, dtype=torch.int32, device=device)
+            ti = torch.zeros((m, k), dtype=torch.int32, device=device)
+            fn(hd, x, am, ws, topk=k, topk_idx=ti)
+            res.append(ti.cpu().numpy())
+        a, c = res
+        agree += int((a[:, 0] == c[:, 0]).sum())
+        overlap += float(np.mean([len(set(a[t]) & set(c[t])) / k for t in range(m)])) * m
+    return {"n": n, "k": k, "top1_agree": agree / n, "topk_mean_overlap": overlap / n,
+            "inputs": "N(0,1) bf16 residuals, RMSNorm'd as in the decode step (seed 16)"}
+
+
+def _rmsnorm_bf16(h):
+    x = h.float()
+    inv = torch.rsqrt((x * x).mean(dim=1, keepdim=True) + 1e-6)
+    return (x * inv).to(torch.bfloat16)
+
+
+def time_sampler(head, st, device, steps: int = 20):
+    """The FP8 head with the draw fused in (temperature 0.6, top_p 0.95, top_k 29) vs the head
+    alone, on the step's final residual: mean µs of each."""
+    from moe_decode_weight_gb300 import api
+    m = st.m
+    u = torch.rand(m, dtype=torch.float64, device=device)
+    tok = torch.zeros(m, dtype=torch.int32, device=device)
+    r = st.resid[st.L]
+    out = {}
+    for name in ("head", "head_draw"):
+        evs = []
+        for i in range(steps + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if name == "head":
+                st.head_call()
+            else:
+                api.lm_head_fp8_sample(head, r, tok, st.hws, u, 0.6, 0.95, TOPK_VOCAB, norm_input=True)
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        out[name + "_us"] = float(np.mean([a.elapsed_time(b) for a, b in evs[3:]])) * 1000
+    return out
+
+
 def run_gpu(args, rank: int, world: int):
     from moe_decode_weight_gb300 import api
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -345,6 +426,11 @@ def run_gpu(args, rank: int, world: int):
                        "verify_cost_ratio": ms4 / ms_step}
         del st4
 
+    if not args.no_extras and args.m == 1:
+        extra["sampler"] = time_sampler(head, st, device)
+        extra["fp8_vs_bf16"] = fp8_vs_bf16(head, _w_bf16, device)
+        extra["sweep"] = sweep(layers, head, device)
+
     if rank != 0:
         return
     cpu = None
@@ -392,6 +478,8 @@ def main():
     ap.add_argument("--layers", type=int, default=L_DEFAULT)
     ap.add_argument("--no-m4", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the sampler timing, the FP8/BF16 agreement and the M sweep")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

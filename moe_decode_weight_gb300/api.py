@@ -30,7 +30,8 @@ SYMBOLS = ["mdw_status_string", "mdw_version", "mdw_moe_workspace_bytes", "mdw_m
            "moe_decode_layer", "quantize_lm_head_fp8", "mdw_lm_head_bf16_init",
            "mdw_lm_head_workspace_bytes", "lm_head_fp8", "lm_head_bf16", "lm_head_fp8_rmsnorm",
            "mdw_stack_workspace_bytes",
-           "moe_decode_stack", "mdw_device_status", "moe_decode_layer_noalloc"]
+           "moe_decode_stack", "mdw_device_status", "moe_decode_layer_noalloc", "mdw_sample_topk",
+           "lm_head_fp8_sample", "moe_decode_stack_routed"]
 
 
 class MdwError(RuntimeError):
@@ -95,10 +96,18 @@ def lib() -> C.CDLL:
     L.moe_decode_stack.restype = C.c_int
     L.moe_decode_stack.argtypes = [C.POINTER(MoeWeightsC), i32, C.POINTER(LMHeadC), i32, vp, vp, vp, vp,
                                    i32, vp, vp, vp, sz, vp]
+    L.moe_decode_stack_routed.restype = C.c_int
+    L.moe_decode_stack_routed.argtypes = [C.POINTER(MoeWeightsC), i32, C.POINTER(LMHeadC), i32, vp, vp, vp, vp,
+                                          i32, vp, vp, vp, vp, sz, vp]
     L.mdw_device_status.restype = C.c_int
     L.mdw_device_status.argtypes = [vp, vp]
     L.moe_decode_layer_noalloc.restype = C.c_int
     L.moe_decode_layer_noalloc.argtypes = [C.POINTER(MoeWeightsC), i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
+    f64 = C.c_double
+    L.mdw_sample_topk.restype = C.c_int
+    L.mdw_sample_topk.argtypes = [i32, i32, vp, vp, f64, f64, vp, vp, vp]
+    L.lm_head_fp8_sample.restype = C.c_int
+    L.lm_head_fp8_sample.argtypes = [C.POINTER(LMHeadC), i32, vp, i32, i32, f64, f64, vp, vp, vp, vp, vp, sz, vp]
     _lib = L
     return L
 
@@ -230,6 +239,24 @@ def lm_head_fp8_rmsnorm(head: LMHead, r: torch.Tensor, argmax_out: torch.Tensor,
     _head("lm_head_fp8_rmsnorm", head, r, argmax_out, ws, logits, topk, topk_idx, topk_val, stream)
 
 
+def mdw_sample_topk(topk_val: torch.Tensor, topk_idx: torch.Tensor, temperature: float, top_p: float,
+                    u: torch.Tensor, token_out: torch.Tensor, stream=None) -> None:
+    """Draw one token per row of the [M, k] candidates (u: float64 [M] uniforms in [0, 1))."""
+    m, k = topk_val.shape
+    _check("mdw_sample_topk", lib().mdw_sample_topk(m, k, _ptr(topk_val), _ptr(topk_idx), float(temperature),
+                                                      float(top_p), _ptr(u), _ptr(token_out), _stream(stream)))
+
+
+def lm_head_fp8_sample(head: LMHead, h: torch.Tensor, token_out: torch.Tensor, ws: torch.Tensor, u: torch.Tensor,
+                       temperature: float, top_p: float, topk: int, norm_input: bool = False, topk_idx=None,
+                       topk_val=None, stream=None) -> None:
+    """FP8 head (optionally on bf16(RMSNorm(h))) and the draw on its top-k, in one launch."""
+    _check("lm_head_fp8_sample",
+           lib().lm_head_fp8_sample(C.byref(head.c), h.shape[0], _ptr(h), 1 if norm_input else 0, topk,
+                                    float(temperature), float(top_p), _ptr(u), _ptr(token_out), _ptr(topk_idx),
+                                    _ptr(topk_val), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def _layer_array(layers):
     """ctypes array of layer descriptors (a prebuilt array is passed through unchanged)."""
     if isinstance(layers, C.Array):
@@ -255,6 +282,19 @@ def moe_decode_stack(layers, head, r0: torch.Tensor, argmax_out, ws: torch.Tenso
                                   _ptr(logits), _ptr(argmax_out), topk, _ptr(topk_idx), _ptr(topk_val),
                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check("moe_decode_stack", code)
+
+
+def moe_decode_stack_routed(layers, head, r0: torch.Tensor, argmax_out, ws: torch.Tensor, topk_override,
+                            resid_out=None, logits=None, topk: int = 1, topk_idx=None, topk_val=None,
+                            stream=None) -> None:
+    """moe_decode_stack with imposed routing: topk_override int32 [L, M, K] on the device (or None)."""
+    arr = _layer_array(layers)
+    hc = C.byref(head.c) if head is not None else None
+    code = lib().moe_decode_stack_routed(arr, len(layers), hc, r0.shape[0], _ptr(r0), _ptr(resid_out),
+                                         _ptr(logits), _ptr(argmax_out), topk, _ptr(topk_idx), _ptr(topk_val),
+                                         _ptr(topk_override), _ptr(ws), ws.numel() * ws.element_size(),
+                                         _stream(stream))
+    _check("moe_decode_stack_routed", code)
 
 
 def mdw_device_status(ws: torch.Tensor, stream=None) -> int:

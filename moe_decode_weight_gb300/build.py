@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmdw.so")
-SOURCES = ["moe.cu", "lm_head.cu", "abi.cu", "noalloc.cu"]
+SOURCES = ["moe.cu", "lm_head.cu", "abi.cu", "noalloc.cu", "sampler.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=default",

@@ -113,10 +113,20 @@ void fill_ws(MoeParams& p, const mdw_moe_ws_layout& l, uint8_t* base) {
   p.sh = reinterpret_cast<float*>(base + l.sh);
 }
 
+struct Draw {                     // optional draw on the final top-k
+  const double* u = nullptr;
+  double temperature = 0.0, top_p = 1.0;
+  int32_t* out = nullptr;
+};
+
 mdw_status head_call(const mdw_lm_head* head, int fmt, int32_t M, const void* h_bf16, int norm_input,
                      float* logits, int32_t* argmax_out, int32_t topk, int32_t* topk_idx,
-                     float* topk_val, uint32_t* hdr, uint8_t* cand, cudaStream_t s) {
+                     float* topk_val, uint32_t* hdr, uint8_t* cand, cudaStream_t s, const Draw& draw = Draw()) {
   HeadParams hp{};
+  hp.sample_u = draw.u;
+  hp.temperature = draw.temperature;
+  hp.top_p = draw.top_p;
+  hp.sample_out = draw.out;
   hp.w = static_cast<const uint8_t*>(head->w);
   hp.row_scale = head->row_scale;
   hp.V = head->vocab;
@@ -137,18 +147,18 @@ mdw_status head_call(const mdw_lm_head* head, int fmt, int32_t M, const void* h_
 
 mdw_status head_entry(int fmt, const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
                       int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val, void* ws,
-                      size_t ws_bytes, cudaStream_t s, int norm_input = 0) {
+                      size_t ws_bytes, cudaStream_t s, int norm_input = 0, const Draw& draw = Draw()) {
   mdw_status st = check_head(head, fmt);
   if (st != MDW_OK) return st;
   if (M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK || head->vocab < topk)
     return MDW_ERR_INVALID_ARG;
-  if (!al16(h_bf16) || !al16_or_null(logits) || !argmax_out || !al16(ws)) return MDW_ERR_INVALID_ARG;
+  if (!al16(h_bf16) || !al16_or_null(logits) || !(argmax_out || draw.out) || !al16(ws)) return MDW_ERR_INVALID_ARG;
   if (ws_bytes < mdw_lm_head_workspace_bytes(head, M, topk)) return MDW_ERR_WORKSPACE_TOO_SMALL;
   if (head_grid() <= 0) return MDW_ERR_CUDA;
   uint8_t* base = static_cast<uint8_t*>(ws);
   if (cudaMemsetAsync(base, 0, kHdrWords * 4, s) != cudaSuccess) return MDW_ERR_CUDA;
   return head_call(head, fmt, M, h_bf16, norm_input, logits, argmax_out, topk, topk_idx, topk_val,
-                   reinterpret_cast<uint32_t*>(base), base + kHdrWords * 4, s);
+                   reinterpret_cast<uint32_t*>(base), base + kHdrWords * 4, s, draw);
 }
 
 }  // namespace
@@ -281,6 +291,22 @@ mdw_status lm_head_fp8_rmsnorm(const mdw_lm_head* head, int32_t M, const void* r
                     ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), 1);
 }
 
+mdw_status lm_head_fp8_sample(const mdw_lm_head* head, int32_t M, const void* h_bf16, int32_t norm_input,
+                              int32_t topk, double temperature, double top_p, const double* u,
+                              int32_t* token_out, int32_t* topk_idx, float* topk_val, void* ws,
+                              size_t ws_bytes, mdw_stream_t stream) {
+  if (!u || !token_out || (reinterpret_cast<uintptr_t>(u) & 7u) != 0 || (reinterpret_cast<uintptr_t>(token_out) & 3u) != 0)
+    return MDW_ERR_INVALID_ARG;
+  if (!(top_p > 0.0 && top_p <= 1.0) || temperature != temperature) return MDW_ERR_INVALID_ARG;
+  Draw d;
+  d.u = u;
+  d.temperature = temperature;
+  d.top_p = top_p;
+  d.out = token_out;
+  return head_entry(MDW_FMT_FP8_E4M3_ROWSCALE, head, M, h_bf16, nullptr, nullptr, topk, topk_idx, topk_val, ws,
+                    ws_bytes, reinterpret_cast<cudaStream_t>(stream), norm_input != 0 ? 1 : 0, d);
+}
+
 size_t mdw_stack_workspace_bytes(const mdw_moe_weights* layers, int32_t L, const mdw_lm_head* head,
                                  int32_t M, int32_t topk) {
   if (!layers || L < 1 || L > kMaxLayers || M < 1 || M > MDW_MAX_M) return 0;
@@ -299,6 +325,14 @@ mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_
                             const void* r0_bf16, void* resid_out, float* logits, int32_t* argmax_out,
                             int32_t topk, int32_t* topk_idx, float* topk_val, void* ws, size_t ws_bytes,
                             mdw_stream_t stream) {
+  return moe_decode_stack_routed(layers, L, head, M, r0_bf16, resid_out, logits, argmax_out, topk, topk_idx,
+                                 topk_val, nullptr, ws, ws_bytes, stream);
+}
+
+mdw_status moe_decode_stack_routed(const mdw_moe_weights* layers, int32_t L, const mdw_lm_head* head, int32_t M,
+                                   const void* r0_bf16, void* resid_out, float* logits, int32_t* argmax_out,
+                                   int32_t topk, int32_t* topk_idx, float* topk_val, const int32_t* topk_override,
+                                   void* ws, size_t ws_bytes, mdw_stream_t stream) {
   if (!layers || L < 1 || L > kMaxLayers) return MDW_ERR_INVALID_ARG;
   mdw_status st = MDW_OK;
   if (head) {
@@ -322,7 +356,9 @@ mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_
                !al16_or_null(logits)))
     return MDW_ERR_INVALID_ARG;
   if (!head) topk = 1;
-  if (!al16(r0_bf16) || !al16_or_null(resid_out) || !al16(ws)) return MDW_ERR_INVALID_ARG;
+  if (!al16(r0_bf16) || !al16_or_null(resid_out) || !al16(ws) ||
+      (reinterpret_cast<uintptr_t>(topk_override) & 3u) != 0)
+    return MDW_ERR_INVALID_ARG;
   const MoeWs lay = moe_ws_layout(M, E, K, true, topk);
   if (ws_bytes < lay.total) return MDW_ERR_WORKSPACE_TOO_SMALL;
   if (moe_grid() * 32 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
@@ -333,6 +369,7 @@ mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_
   p->L = L; p->M = M; p->E = E; p->K = K;
   p->has_shared = layers[0].sh_w13_q != nullptr;
   p->stack_mode = 1;
+  p->topk_override = topk_override;
   p->r0 = static_cast<const __nv_bfloat16*>(r0_bf16);
   if (resid_out) {
     p->resid = static_cast<__nv_bfloat16*>(resid_out);

@@ -16,6 +16,7 @@
 // and the last block to finish merges all blocks' lists.
 #include "mdw_device.cuh"
 #include "mdw_internal.h"
+#include "mdw_sampler.cuh"
 
 namespace mdw {
 namespace {
@@ -608,10 +609,20 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
     if (lane < tk) {
       const float v = lv[t * kWarps * kMaxTK + lane];
       const int i = li[t * kWarps * kMaxTK + lane];
-      if (lane == 0) p.argmax_out[t] = i;
+      if (lane == 0 && p.argmax_out) p.argmax_out[t] = i;
       if (p.topk_idx) p.topk_idx[(size_t)t * tk + lane] = i;
       if (p.topk_val) p.topk_val[(size_t)t * tk + lane] = v;
     }
+  if (p.sample_u) {
+    // the draw on the final top-k (one warp per token, candidates in shared memory)
+    for (int t = warp; t < M; t += kWarps) {
+      const float* cv = lv + t * kWarps * kMaxTK;
+      const int* ci = li + t * kWarps * kMaxTK;
+      const int32_t tok = sample_candidates_warp([&](int i) { return cv[i]; }, [&](int i) { return ci[i]; }, tk,
+                                                 p.temperature, p.top_p, p.sample_u[t], lane);
+      if (lane == 0) p.sample_out[t] = tok;
+    }
+  }
   MDW_HEAD_TRACE(threadIdx.x == 0, 6);
 }
 

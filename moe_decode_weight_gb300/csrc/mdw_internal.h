@@ -82,6 +82,9 @@ struct HeadParams {
   int32_t* topk_idx;           // [M][topk] or null
   float* topk_val;             // [M][topk] or null
   uint32_t* hdr;               // header (status, done counter)
+  const double* sample_u;      // [M] uniforms in [0, 1), or null: no draw
+  double temperature, top_p;   // draw settings (used when sample_u is set)
+  int32_t* sample_out;         // [M] drawn token ids
   float* cand_val;             // [grid + kHeadMaxGroups][M][topk]: block lists, then group lists
   int32_t* cand_idx;           // [grid + kHeadMaxGroups][M][topk]
 };

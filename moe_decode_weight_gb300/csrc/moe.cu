@@ -284,12 +284,14 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) tb.bad = 0;
   if (p.topk_override) {
+    // imposed routing: [M][K] for one layer, [L][M][K] for the stack
+    const int32_t* ov = p.topk_override + (p.stack_mode ? (size_t)layer * M * K : 0);
     for (int t = warp; t < M; t += kWarps) {
       if (lane < K) {
-        int id = p.topk_override[t * K + lane];
+        int id = ov[t * K + lane];
         bool ok = id >= 0 && id < E;
         for (int j = 0; j < K; ++j)
-          if (j != lane && p.topk_override[t * K + j] == id) ok = false;
+          if (j != lane && ov[t * K + j] == id) ok = false;
         if (!ok) { atomicExch(&tb.bad, 1); id = 0; }
         tb.ids[t * K + lane] = id;
         tb.gts[t * K + lane] = ld_cg_f32(p.logits + (size_t)t * E + id);
