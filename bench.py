@@ -375,6 +375,23 @@ def time_sampler(head, st, device, steps: int = 20):
     return out
 
 
+def moe_traffic(layers: int, m: int):
+    """DRAM bytes (read + write) of one stack launch from the committed ncu capture, scaled
+    by the layer count; None unless the kernel sources still hash to the captured ones and
+    the bench runs the captured M."""
+    import hashlib
+    try:
+        meta = json.load(open(os.path.join(ROOT, "profiles", "moe_traffic.json")))
+        h = hashlib.sha256()
+        for f in meta["sources"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != meta["sources_sha256"] or m != 1:
+            return None
+        return float(meta["dram_bytes_per_layer_m1"]) * layers
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def run_gpu(args, rank: int, world: int):
     from moe_decode_weight_gb300 import api
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -455,7 +472,8 @@ def run_gpu(args, rank: int, world: int):
         "layer_stack_gbs": lay_gbs, "head_us": head_ms * 1000, "head_gbs": head_gbs,
         "bytes_per_step": b_step,
         "roofline": {"bound": "hbm", "achieved": lay_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": lay_gbs / peak, "traffic": None,
+                     "frac": lay_gbs / peak, "traffic": moe_traffic(args.layers, args.m),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "kernel": "moe_persistent_kernel (42 layers, one launch)",
                      "peak_kind": peak_kind},
         "cpu_baseline": cpu,

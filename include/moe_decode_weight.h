@@ -292,8 +292,8 @@ mdw_status lm_head_fp8_rmsnorm(const mdw_lm_head* head, int32_t M, const void* r
                                int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val,
                                void* ws, size_t ws_bytes, mdw_stream_t stream);
 
-/* Decode-time draw on top-k candidates ("NVIDIA DGX Spark MoE inference: three
- * optimizations", section "GSM8K measured a 42.5% throughput gain across 1,319 questions":
+/* Decode-time draw on top-k candidates ("Three MoE Inference Optimizations NVIDIA
+ * Measured on DGX Spark", section "GSM8K measured a 42.5% throughput gain across 1,319 questions":
  * temperature 0.6, top_p 0.95, top_k 29). The pages give the settings only; the steps
  * (reading): per token, e_i = exp((z_i - z_0) / temperature) over the k candidates in head
  * order; keep the shortest prefix whose mass reaches top_p * total (the crossing candidate

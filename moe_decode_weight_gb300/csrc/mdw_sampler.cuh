@@ -1,7 +1,7 @@
 // The decode-time draw on the LM head's top-k candidates: temperature, nucleus (top_p) and
 // one inverse-CDF draw per token.
 //
-// Method: blog.neticslabs.com, "NVIDIA DGX Spark MoE inference: three optimizations",
+// Method: "Three MoE Inference Optimizations NVIDIA Measured on DGX Spark",
 // section "GSM8K measured a 42.5% throughput gain across 1,319 questions" -- the evaluation
 // samples at temperature 0.6, top_p 0.95, top_k 29 (also runbyai.xyz/posts/593, paragraph
 // 6). The pages give only the settings; the steps are the plain reading:

@@ -17,17 +17,23 @@
 //
 // Execution model (GB300, one block of 384 threads per SM, cooperative launch):
 //   per layer, every block
-//   P0  (stack) x = bf16(RMSNorm(r_l)) and (all) xq = E4M3(x / sx): computed redundantly
-//       by every block from the 5 KB/token input, so no exchange is needed;
-//   P1  router logits for its slice of the E router rows -> global; arrive(B1);
-//       while B1 completes: the shared expert's gate/up for its static slice of rows;
-//   P2  wait(B1); top-k + dedup redundantly from the E x M logits (every block derives
-//       the same slot / pair tables); L2 prefetch of its down-projection rows;
-//   P3  routed gate/up for its contiguous slice of the (slot, row-pair) space -> h;
-//       arrive(B2); (stack) L2 prefetch of the next layer's static weights; wait(B2);
+//   P0  the weights of its router row are requested first; (stack) x = bf16(RMSNorm(r_l))
+//       and (all) xq = E4M3(x / sx), computed redundantly by every block from the 5 KB/token
+//       input, so no exchange is needed;
+//   P1  router logits for its slice of the E router rows -> global; B1;
+//   P2  top-k + dedup redundantly from the E x M logits (every block derives the same slot /
+//       pair tables; slot 0 is the shared expert); as soon as the slots are known, warps
+//       1.. issue bulk L2 prefetches of every weight byte the block reads in the layer
+//       while warp 0 finishes the pair tables;
+//   P3  gate/up for its contiguous share of the (slot, row-pair) space -> h; arrive(B2);
+//       (stack) L2 prefetch of the next layer's static weights; wait(B2);
 //   P4  every block quantises all pairs' h (amax / 448) into shared memory, then computes
 //       its slice of output rows over all slots (no atomics: a fixed summation order);
 //       (stack) r_{l+1} = bf16(r_l + y); B3.
+//   The expert GEMVs run on m16n8k16 tensor-core MMAs: with at most two tokens the MMA
+//   columns carry (token, K-block) pairs (block-column form, scales applied per column in
+//   fp32); with more tokens they carry tokens, the E8M0 scale folded into the f16 weights
+//   when that is exact (token-column form).
 // Every inter-block wait is bounded and records MDW_ERR_TIMEOUT instead of hanging.
 #include "mdw_device.cuh"
 #include "mdw_internal.h"

@@ -5,7 +5,7 @@ Test infrastructure (see ``oracle/__init__.py``).
 
 Sources (page title, section):
 
-* blog.neticslabs.com, "NVIDIA DGX Spark MoE inference: three optimizations", section
+* "Three MoE Inference Optimizations NVIDIA Measured on DGX Spark", section
   "GSM8K measured a 42.5% throughput gain across 1,319 questions": the evaluation samples
   at temperature 0.6 with top_p 0.95 and top_k 29.
 * runbyai.xyz/posts/593, paragraph 6: the same three settings, against greedy decoding on
