@@ -47,10 +47,10 @@ constexpr int kW2RowBytes = kI / 2;             // 384
 constexpr int kXhBytes = kH * 2 + 64;           // f16 x-hat per token, padded (conflict-free B loads)
 constexpr int kGuRound = 4 * kWarps;            // gate/up units per round (partials in smem)
 constexpr int kGuMaxTiles = 320;                // (tile, token-tile) entries per block
-constexpr int kMaxSegs = 32;                    // slot segments per block list
+constexpr int kMaxSegs = 48;                    // slot segments per block list (>= kPairChunk + 1)
 constexpr int kTopkCand = 128;                  // compacted top-k candidates per warp
 constexpr int kHhBytes = kI * 2 + 64;           // f16 h-hat per pair, padded (conflict-free A loads)
-constexpr int kPairChunk = 24;                  // pairs quantised into smem at a time
+constexpr int kPairChunk = 36;                  // pairs quantised into smem at a time (all of M = 4)
 // per-warp cp.async rings (16-byte asynchronous copies into padded, bank-conflict-free rows)
 constexpr int kGuU = 8;                         // gate/up: 32-blocks per stage
 constexpr int kGuStages = 3;
@@ -281,8 +281,6 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
 
 // ------------------------------------------------------------------ P2: top-k + dedup
 
-__device__ void prefetch_block_weights(const MoeParams& p, const LayerDesc& L, const Tables& tb, int a, int b);
-
 __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb, int layer, uint8_t* scratch) {
   const int M = p.M, E = p.E, K = p.K;
   // per-warp candidate buffers live in the gate/up partial-sum region (not live during
@@ -388,8 +386,7 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
   if (tb.bad) return;
   // Routing tables (warp 0): gates, the union of the selections and its slots (slot 0 = shared
   // expert when present, then the union ascending); then the pairs (slot-major,
-  // token-minor). Between the two, the block's gate/up share is known, and the other warps
-  // ask L2 for its weights while warp 0 finishes the pair tables.
+  // token-minor).
   const int first = p.has_shared ? 1 : 0;
   auto slot_of = [&](int e) {
     return first + tb.wpre[e >> 5] + __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
@@ -481,10 +478,6 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
     }
     if (p.has_shared)
       for (int t = lane; t < M; t += 32) { tb.pair_token[t] = t; tb.pair_slot[t] = 0; tb.pair_gate[t] = 1.0f; }
-  } else {
-    const long long PR = (long long)S * kI;
-    const int G = gridDim.x;
-    prefetch_block_weights(p, L, tb, (int)((long long)blockIdx.x * PR / G), (int)((long long)(blockIdx.x + 1) * PR / G));
   }
   __syncthreads();
   if (blockIdx.x == 0) {
@@ -774,11 +767,14 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
   const int g = lane >> 2, q = lane & 3;
   float4* red = reinterpret_cast<float4*>(const_cast<uint8_t*>(smem) + smem_layout(p.M).gured);
   // K split per tile: ks parts of 10 / ks stages (8 blocks each), chosen to minimise the
-  // stages of the busiest warp, ceil(tiles * ks / warps) * 10 / ks (ties: the smaller ks)
+  // busiest warp's stages, ceil(tiles * ks / warps) * 10 / ks, plus about three stages of
+  // latency and epilogue per round of kGuRound units (ties: the smaller ks)
   int ks = 1, best = 1 << 30;
   for (int c = 1; c <= 10; ++c) {
     if (10 % c != 0) continue;
-    const int cost = (tb.gu_n * c + kWarps - 1) / kWarps * (10 / c);
+    const int per_round = kGuRound / c * c;
+    const int rounds = (tb.gu_n * c + per_round - 1) / per_round;
+    const int cost = (tb.gu_n * c + kWarps - 1) / kWarps * (10 / c) + 3 * rounds;
     if (cost < best) { best = cost; ks = c; }
   }
   const int units = tb.gu_n * ks;
@@ -907,31 +903,36 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     quantise_pairs(p, smem, tb, q0, n);
     MDW_TRACE_POINT(layer, 18);
     // unit list: (slot, full tile, K half, 8-token group)
-    // the slots of the chunk (at most kPairChunk + 1 <= 32: one per lane of warp 0) and their
-    // unit counts (tiles x 8-pair groups x 2 K halves), scanned; then every thread writes units
+    // the slots of the chunk (at most kPairChunk + 1, 32 per round of warp 0) and their unit
+    // counts (tiles x 8-pair groups x 2 K halves), scanned; then every thread writes units
+    static_assert(kMaxSegs >= kPairChunk + 1, "segment tables too small for a pair chunk");
     if (warp == 0) {
       const int s_lo = tb.pair_slot[q0], s_hi = tb.pair_slot[q0 + n - 1];
-      const int sidx = s_lo + lane;
-      int c = 0, pa = 0;
-      if (sidx <= s_hi) {
-        pa = max(tb.slot_begin[sidx], q0);
-        const int pz = min(tb.slot_begin[sidx + 1], q0 + n);
-        c = nfull * ((pz - pa + 7) / 8) * 2;
-      }
-      int incl = c;
+      int carry = 0;
+      for (int b0 = 0; s_lo + b0 <= s_hi; b0 += 32) {
+        const int sidx = s_lo + b0 + lane;
+        int c = 0, pa = 0;
+        if (sidx <= s_hi) {
+          pa = max(tb.slot_begin[sidx], q0);
+          const int pz = min(tb.slot_begin[sidx + 1], q0 + n);
+          c = nfull * ((pz - pa + 7) / 8) * 2;
+        }
+        int incl = c;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += nb;
-      }
-      if (sidx <= s_hi) {
-        tb.seg_slot[lane] = sidx;
-        tb.seg_lo[lane] = pa;
-        tb.seg_groups[lane] = c / (2 * max(1, nfull));
-        tb.seg_off[lane] = incl - c;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += nb;
+        }
+        if (sidx <= s_hi) {
+          tb.seg_slot[b0 + lane] = sidx;
+          tb.seg_lo[b0 + lane] = pa;
+          tb.seg_groups[b0 + lane] = c / (2 * max(1, nfull));
+          tb.seg_off[b0 + lane] = carry + incl - c;
+        }
+        if (sidx == s_hi) { tb.seg_off[b0 + lane + 1] = carry + incl; tb.gu_n = carry + incl; }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) tb.n_segs = s_hi - s_lo + 1;
-      if (sidx == s_hi) { tb.seg_off[lane + 1] = incl; tb.gu_n = incl; }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < tb.gu_n; i += blockDim.x) {
@@ -1140,35 +1141,24 @@ __device__ __forceinline__ void prefetch_bulk(const uint8_t* base, size_t lo, si
   if (hi > lo) prefetch_l2(base + lo, (uint32_t)(hi - lo));
 }
 
-// L2 prefetch of every weight byte the block reads in the layer, as soon as the slots are
-// known: its gate/up row pairs [a, b) of the slot space (gate rows, up rows, their scales)
-// first, then its W2 rows [r0, r1) (and scales) of every slot. The contiguous ranges are
-// dealt to lane 0 of warps 1, 2, ... (warp 0 is building the routing tables meanwhile).
-__device__ void prefetch_block_weights(const MoeParams& p, const LayerDesc& L, const Tables& tb, int a, int b) {
+// Bulk L2 prefetches are accepted by the TMA unit only as fast as the memory system takes
+// their requests, so the issuing thread (and its warp) blocks for about (bytes in flight
+// GPU-wide) / (DRAM bandwidth). The W2 rows are therefore requested after the block has
+// arrived at the h barrier, where the blocking overlaps the wait; the gate/up rows are not
+// prefetched at all (measured: requesting them right after routing delayed the warps that
+// issued them by more than the cp.async pipeline gained).
+// The block's W2 rows [r0, r1) (and scales) of every slot, dealt to every warp's lane 0.
+__device__ void prefetch_down_rows(const LayerDesc& L, const Tables& tb) {
   const int G = gridDim.x;
   const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) != 0 || warp == 0) return;
-  int k = 0;
-  auto mine = [&]() { return 1 + k++ % (kWarps - 1) == warp; };
-  while (a < b) {
-    const int slot = a / kI, ja = a % kI, jb = min(kI, ja + (b - a));
-    const int e = tb.slot_expert[slot];
-    const uint8_t* q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
-    const uint8_t* s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
-    for (int half = 0; half < 2; ++half) {
-      const size_t row = (size_t)half * kI;
-      if (mine()) prefetch_bulk(q13, (row + ja) * kW13RowBytes, (row + jb) * kW13RowBytes);
-      if (mine()) prefetch_bulk(s13, (row + ja) * kHBlocks, (row + jb) * kHBlocks);
-    }
-    a += jb - ja;
-  }
+  if ((threadIdx.x & 31) != 0) return;
   const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
-  for (int s = 0; s < tb.n_slots; ++s) {
+  for (int s = warp; s < tb.n_slots; s += kWarps) {
     const int e = tb.slot_expert[s];
     const uint8_t* q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
     const uint8_t* s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
-    if (mine()) prefetch_bulk(q2, (size_t)r0 * kW2RowBytes, (size_t)r1 * kW2RowBytes);
-    if (mine()) prefetch_bulk(s2, (size_t)r0 * kIBlocks, (size_t)r1 * kIBlocks);
+    prefetch_bulk(q2, (size_t)r0 * kW2RowBytes, (size_t)r1 * kW2RowBytes);
+    prefetch_bulk(s2, (size_t)r0 * kIBlocks, (size_t)r1 * kIBlocks);
   }
 }
 
@@ -1231,6 +1221,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);
+    prefetch_down_rows(L, tb);
     if (p.stack_mode && layer + 1 < p.L) prefetch_static(p, p.layers[layer + 1]);
     if (!bar.wait()) return;
     MDW_TRACE_POINT(layer, 7);
