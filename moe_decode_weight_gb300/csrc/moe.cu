@@ -445,10 +445,10 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
       if (p.has_shared) tb.slot_expert[0] = -1;
     }
   }
-  __syncthreads();
   MDW_TRACE_POINT(layer, 11);
-  const int S = tb.n_slots;
   if (warp == 0) {
+    __syncwarp();
+    const int S = tb.n_slots;
     // token masks of the routed slots -> counts -> slot_begin (scan) -> pair positions: the
     // pairs of a slot are token-ordered, so a pair's rank is the number of the slot's earlier
     // tokens, popc(mask & ((1 << t) - 1))
@@ -876,8 +876,60 @@ __device__ void quantise_pairs(const MoeParams& p, uint8_t* smem, Tables& tb, in
 //  * Leftover rows (nrows mod 16) on the CUDA cores, one warp per (slot, row).
 // Every (pair, row) result is multiplied by the pair's gate and h scale into `part`, and the
 // per-token sums are taken in pair order, so the output does not depend on scheduling.
+// Down-projection unit list of pairs [q0, q0 + n): (slot, full 16-row tile, K half, 8-pair
+// group). The slots of the chunk (at most kPairChunk + 1, 32 per round of warp 0) and their
+// unit counts (tiles x 8-pair groups x 2 K halves) are scanned; then every thread writes
+// units. Every thread of the block must call it.
+__device__ void build_down_units(Tables& tb, int q0, int n, int nfull) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  static_assert(kMaxSegs >= kPairChunk + 1, "segment tables too small for a pair chunk");
+  if (warp == 0) {
+    const int s_lo = tb.pair_slot[q0], s_hi = tb.pair_slot[q0 + n - 1];
+    int carry = 0;
+    for (int b0 = 0; s_lo + b0 <= s_hi; b0 += 32) {
+      const int sidx = s_lo + b0 + lane;
+      int c = 0, pa = 0;
+      if (sidx <= s_hi) {
+        pa = max(tb.slot_begin[sidx], q0);
+        const int pz = min(tb.slot_begin[sidx + 1], q0 + n);
+        c = nfull * ((pz - pa + 7) / 8) * 2;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      if (sidx <= s_hi) {
+        tb.seg_slot[b0 + lane] = sidx;
+        tb.seg_lo[b0 + lane] = pa;
+        tb.seg_groups[b0 + lane] = c / (2 * max(1, nfull));
+        tb.seg_off[b0 + lane] = carry + incl - c;
+      }
+      if (sidx == s_hi) { tb.seg_off[b0 + lane + 1] = carry + incl; tb.gu_n = carry + incl; }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tb.n_segs = s_hi - s_lo + 1;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < tb.gu_n; i += blockDim.x) {
+    int k = 0;
+    while (i >= tb.seg_off[k + 1]) ++k;
+    const int r = i - tb.seg_off[k], gq = tb.seg_groups[k];
+    const int kp = r & 1, tg = r >> 1;
+    tb.gu_tile[i] = make_int4(tb.seg_slot[k], tg / gq, kp, tb.seg_lo[k] + 8 * (tg % gq));
+  }
+  __syncthreads();
+}
+
+// Output rows [r0, r1) of this block: 16-row tiles + a remainder.
+__device__ __forceinline__ int down_full_tiles(int G) {
+  const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
+  return (r1 - r0) / 16;
+}
+
 __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* smem, Tables& tb,
-                             int layer) {
+                             int layer, bool first_list_ready) {
   const int M = p.M, G = gridDim.x;
   const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
   const int nrows = r1 - r0, nfull = nrows / 16, nrem = nrows - 16 * nfull;
@@ -902,47 +954,10 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     MDW_TRACE_POINT(layer, 17);
     quantise_pairs(p, smem, tb, q0, n);
     MDW_TRACE_POINT(layer, 18);
-    // unit list: (slot, full tile, K half, 8-token group)
-    // the slots of the chunk (at most kPairChunk + 1, 32 per round of warp 0) and their unit
-    // counts (tiles x 8-pair groups x 2 K halves), scanned; then every thread writes units
-    static_assert(kMaxSegs >= kPairChunk + 1, "segment tables too small for a pair chunk");
-    if (warp == 0) {
-      const int s_lo = tb.pair_slot[q0], s_hi = tb.pair_slot[q0 + n - 1];
-      int carry = 0;
-      for (int b0 = 0; s_lo + b0 <= s_hi; b0 += 32) {
-        const int sidx = s_lo + b0 + lane;
-        int c = 0, pa = 0;
-        if (sidx <= s_hi) {
-          pa = max(tb.slot_begin[sidx], q0);
-          const int pz = min(tb.slot_begin[sidx + 1], q0 + n);
-          c = nfull * ((pz - pa + 7) / 8) * 2;
-        }
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += nb;
-        }
-        if (sidx <= s_hi) {
-          tb.seg_slot[b0 + lane] = sidx;
-          tb.seg_lo[b0 + lane] = pa;
-          tb.seg_groups[b0 + lane] = c / (2 * max(1, nfull));
-          tb.seg_off[b0 + lane] = carry + incl - c;
-        }
-        if (sidx == s_hi) { tb.seg_off[b0 + lane + 1] = carry + incl; tb.gu_n = carry + incl; }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) tb.n_segs = s_hi - s_lo + 1;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < tb.gu_n; i += blockDim.x) {
-      int k = 0;
-      while (i >= tb.seg_off[k + 1]) ++k;
-      const int r = i - tb.seg_off[k], gq = tb.seg_groups[k];
-      const int kp = r & 1, tg = r >> 1;
-      tb.gu_tile[i] = make_int4(tb.seg_slot[k], tg / gq, kp, tb.seg_lo[k] + 8 * (tg % gq));
-    }
-    __syncthreads();
+    // unit list (the first chunk's was built during the h barrier); either way a block-wide
+    // barrier follows, so every warp sees the whole chunk's h-hat before the tiles
+    if (q0 > 0 || !first_list_ready) build_down_units(tb, q0, n, nfull);
+    else __syncthreads();
     MDW_TRACE_POINT(layer, 13);
     // leftover rows (nrows mod 16, CUDA cores, one warp per (pair, row)): the weights of
     // this warp's first item are requested now, so they arrive while the tiles run
@@ -1209,10 +1224,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
     __syncthreads();
     if (tb.bad) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
     {
-      // gate/up row pairs of every slot (the shared expert is slot 0), dealt to the blocks
-      // in equal contiguous shares
-      const long long PR = (long long)tb.n_slots * kI;
-      const int a = (int)((long long)blockIdx.x * PR / G), b = (int)((long long)(blockIdx.x + 1) * PR / G);
+      // gate/up tiles of 8 row pairs of every slot (the shared expert is slot 0; 96 whole
+      // tiles per slot), dealt to the blocks in equal contiguous shares of whole tiles, so no
+      // block pays for a tile cut at a share boundary
+      const long long T = (long long)tb.n_slots * (kI / 8);
+      const int a = 8 * (int)((long long)blockIdx.x * T / G), b = 8 * (int)((long long)(blockIdx.x + 1) * T / G);
       MDW_TRACE_POINT(layer, 12);
       MDW_TRACE_POINT(layer, 5);
       build_gate_up_tiles(tb, a, b);
@@ -1221,11 +1237,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);
+    // during the h barrier: W2 rows into L2, the first chunk's down unit list (the gate/up
+    // tile list it overwrites is finished), and the next layer's static weights
     prefetch_down_rows(L, tb);
+    build_down_units(tb, 0, min(kPairChunk, tb.n_pairs), down_full_tiles(G));
     if (p.stack_mode && layer + 1 < p.L) prefetch_static(p, p.layers[layer + 1]);
     if (!bar.wait()) return;
     MDW_TRACE_POINT(layer, 7);
-    down_combine(p, L, smem, tb, layer);
+    down_combine(p, L, smem, tb, layer, true);
     MDW_TRACE_POINT(layer, 8);
     if (p.stack_mode && layer + 1 < p.L) {
       if (!bar.sync()) return;                                      // B3 (r_{l+1})
