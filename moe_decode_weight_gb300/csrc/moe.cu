@@ -941,6 +941,14 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
   float4* red = reinterpret_cast<float4*>(smem + sl.gured);
   uint8_t* ring = smem + sl.ring + (size_t)warp * warp_ring_bytes(M);
   for (int i = threadIdx.x; i < M * kMaxRowsPerBlock; i += blockDim.x) yacc[i] = 0.f;
+  // the residual of this thread's first output element, requested now (its load overlaps
+  // the whole projection instead of following it)
+  const __nv_bfloat16* res_in = p.stack_mode ? resid_ptr(p, layer) : p.residual;
+  float res0 = 0.f;
+  if (res_in && threadIdx.x < M * nrows) {
+    const int t = threadIdx.x / nrows, rr = threadIdx.x % nrows;
+    res0 = __bfloat162float(res_in[(size_t)t * kH + r0 + rr]);
+  }
   auto w2_of = [&](int slot, const uint8_t*& q2, const uint8_t*& s2) {
     const int e = tb.slot_expert[slot];
     q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
@@ -962,15 +970,41 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     // leftover rows (nrows mod 16, CUDA cores, one warp per (pair, row)): the weights of
     // this warp's first item are requested now, so they arrive while the tiles run
     const int rem_items = n * nrem;
+    const int rem_first = kWarps - 1 - warp;         // the last warps (fewest tiles) start
     uint4 rem_w = make_uint4(0, 0, 0, 0);
     uint32_t rem_s = 0;
-    if (warp < rem_items && lane < kIBlocks) {
-      const int k2 = warp / nrem, rr = 16 * nfull + warp % nrem;
+    if (rem_first < rem_items && lane < kIBlocks) {
+      const int k2 = rem_first / nrem, rr = 16 * nfull + rem_first % nrem;
       const uint8_t *q2, *s2;
       w2_of(tb.pair_slot[q0 + k2], q2, s2);
       rem_w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
       rem_s = ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane);
     }
+    // leftover rows: lanes 0..23 one block each; run by each warp right after its tiles
+    auto do_rem = [&]() {
+    for (int it = rem_first; it < rem_items; it += kWarps) {
+      const int k2 = it / nrem, rr = 16 * nfull + it % nrem, q = q0 + k2;
+      float dsum = 0.f;
+      if (lane < kIBlocks) {
+        if (it != rem_first) {
+          const uint8_t *q2, *s2;
+          w2_of(tb.pair_slot[q], q2, s2);
+          rem_w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
+          rem_s = ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane);
+        }
+        const uint8_t* hh = smem + sl.hh + (size_t)k2 * kHhBytes + 64 * lane;
+        uint32_t x2[16];
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(hh + 16 * pl);
+          x2[4 * pl] = xv.x; x2[4 * pl + 1] = xv.y; x2[4 * pl + 2] = xv.z; x2[4 * pl + 3] = xv.w;
+        }
+        dsum = mx_block_dot(rem_w, x2) * e8m0_to_f32(rem_s);
+      }
+      dsum = warp_sum(dsum);
+      if (lane == 0) part[k2 * kMaxRowsPerBlock + rr] = dsum * tb.sh[k2] * tb.pair_gate[q];
+    }
+    };
     const int units = tb.gu_n;
     for (int u0 = 0; u0 < units; u0 += kGuRound) {
       const int un = min(kGuRound, units - u0);
@@ -1075,6 +1109,7 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
         __syncwarp();
         red[(warp + k * kWarps) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       }
+      if (u0 + kGuRound >= units) do_rem();          // the last round: leftover rows next
       __syncthreads();
       MDW_TRACE_POINT(layer, 19);
       // K halves added in order (unit kp = 0 owns the pair); D rows = W2 rows g, g + 8;
@@ -1096,29 +1131,7 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
         }
       }
     }
-    // leftover rows: lanes 0..23 one block each
-    for (int it = warp; it < rem_items; it += kWarps) {
-      const int k2 = it / nrem, rr = 16 * nfull + it % nrem, q = q0 + k2;
-      float dsum = 0.f;
-      if (lane < kIBlocks) {
-        if (it != warp) {
-          const uint8_t *q2, *s2;
-          w2_of(tb.pair_slot[q], q2, s2);
-          rem_w = ldg_stream16(q2 + (size_t)(r0 + rr) * kW2RowBytes + lane * 16);
-          rem_s = ldg_stream_u8(s2 + (size_t)(r0 + rr) * kIBlocks + lane);
-        }
-        const uint8_t* hh = smem + sl.hh + (size_t)k2 * kHhBytes + 64 * lane;
-        uint32_t x2[16];
-#pragma unroll
-        for (int pl = 0; pl < 4; ++pl) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(hh + 16 * pl);
-          x2[4 * pl] = xv.x; x2[4 * pl + 1] = xv.y; x2[4 * pl + 2] = xv.z; x2[4 * pl + 3] = xv.w;
-        }
-        dsum = mx_block_dot(rem_w, x2) * e8m0_to_f32(rem_s);
-      }
-      dsum = warp_sum(dsum);
-      if (lane == 0) part[k2 * kMaxRowsPerBlock + rr] = dsum * tb.sh[k2] * tb.pair_gate[q];
-    }
+    if (units == 0) do_rem();
     __syncthreads();
     MDW_TRACE_POINT(layer, 14);
     // fixed-order accumulation over the chunk's pairs (ascending)
@@ -1135,13 +1148,13 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     const int t = i / nrows, rr = i % nrows;
     const float y = yacc[t * kMaxRowsPerBlock + rr];
     const size_t o = (size_t)t * kH + r0 + rr;
+    const float rv = (i == (int)threadIdx.x) ? res0 : (res_in ? __bfloat162float(res_in[o]) : 0.f);
     if (p.stack_mode) {
-      const __nv_bfloat16* rin = resid_ptr(p, layer);
       __nv_bfloat16* rout = const_cast<__nv_bfloat16*>(resid_ptr(p, layer + 1));
-      rout[o] = __float2bfloat16_rn(__bfloat162float(rin[o]) + y);
+      rout[o] = __float2bfloat16_rn(rv + y);
     } else {
       float v = y;
-      if (p.residual) v += __bfloat162float(p.residual[o]);
+      if (p.residual) v += rv;
       if (p.y_fp32) reinterpret_cast<float*>(p.y_out)[o] = v;
       else reinterpret_cast<__nv_bfloat16*>(p.y_out)[o] = __float2bfloat16_rn(v);
     }
