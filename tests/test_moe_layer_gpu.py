@@ -223,7 +223,8 @@ def test_device_weights_match_host_regeneration(layer512):
 def _widen_scales(s: torch.Tensor) -> torch.Tensor:
     """Move two thirds of the rows' E8M0 scales outside [113, 140] (the range in which the
     kernels fold the scale into their f16 weights): rows with row % 3 == 0 get 105..112
-    (2^-22 .. 2^-15), row % 3 == 1 get 141..145 (2^14 .. 2^18), the rest keep theirs. A row
+    (2^-22 .. 2^-15), row % 3 == 1 get 141..145 (2^14 .. 2^18), the rest keep theirs, and
+    block 0 of every seventh row gets code 0 (2^-127). A row
     stays within one regime, so its dot products keep an fp32-friendly dynamic range (gate
     row j and up row 768 + j share a regime). Works on [.., rows, blocks] tensors."""
     rows, blocks = s.shape[-2], s.shape[-1]
@@ -232,7 +233,10 @@ def _widen_scales(s: torch.Tensor) -> torch.Tensor:
     k = (r % 3).expand(rows, blocks)
     lo = (105 + (r + b) % 8).to(torch.uint8)
     hi = (141 + (r + b) % 5).to(torch.uint8)
-    return torch.where(k == 0, lo, torch.where(k == 1, hi, s))
+    out = torch.where(k == 0, lo, torch.where(k == 1, hi, s))
+    # code 0 (2^-127, no normal float) in block 0 of every seventh row
+    zero = ((r % 7 == 3) & (b == 0)).expand(rows, blocks)
+    return torch.where(zero, torch.zeros_like(out), out)
 
 
 class WideScaleLayer(Layer):
