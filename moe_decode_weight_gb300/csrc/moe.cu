@@ -281,6 +281,73 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
 
 // ------------------------------------------------------------------ P2: top-k + dedup
 
+// Block 0 publishes the routing of the layer (inspection and the optional outputs).
+__device__ void publish_routing(const MoeParams& p, const Tables& tb, int layer) {
+  const int M = p.M, K = p.K;
+  for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
+    p.ids[i] = tb.ids[i];
+    p.gates[i] = tb.gts[i];
+    if (p.ids_out) p.ids_out[i] = tb.ids[i];
+    if (p.gates_out) p.gates_out[i] = tb.gts[i];
+  }
+  for (int s = threadIdx.x; s < tb.n_slots; s += blockDim.x) p.slot_expert[s] = tb.slot_expert[s];
+  for (int q = threadIdx.x; q < tb.n_pairs; q += blockDim.x) {
+    p.pair_token[q] = tb.pair_token[q];
+    p.pair_slot[q] = tb.pair_slot[q];
+    p.pair_gate[q] = tb.pair_gate[q];
+  }
+  if (threadIdx.x == 0) {
+    p.hdr[kHdrSlots] = tb.n_slots;
+    p.hdr[kHdrPairs] = tb.n_pairs;
+    p.hdr[kHdrRouted] = tb.n_routed;
+    if (layer < kHdrWords - kHdrUnions) p.hdr[kHdrUnions + layer] = tb.n_routed;
+  }
+}
+
+// Routing tables of one token (M == 1), by warp 0 in registers: the gates (softmax of the K
+// selected logits, the same K-lane butterflies as the general tables), the union (the K
+// distinct ids ascending, slots first..first+K-1) and one pair per slot.
+__device__ void routing_tables_one(Tables& tb, int K, int first, int lane) {
+  const bool act = lane < K;
+  const int id = act ? tb.ids[lane] : 0x7fffffff;
+  const float z = act ? tb.gts[lane] : 0.f;
+  float gate;
+  if ((K & (K - 1)) == 0) {
+    float mx = z;
+    for (int o = 1; o < K; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float ez = expf(z - mx);
+    float sum = ez;
+    for (int o = 1; o < K; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    gate = ez / sum;
+  } else {
+    float mx = tb.gts[0];
+    for (int r = 1; r < K; ++r) mx = fmaxf(mx, tb.gts[r]);
+    float sum = 0.f;
+    for (int r = 0; r < K; ++r) sum += expf(tb.gts[r] - mx);
+    gate = act ? expf(z - mx) / sum : 0.f;
+  }
+  int rank = 0;
+  for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, id, j) < id);
+  __syncwarp();
+  const int S = K + first;
+  if (act) {
+    const int slot = first + rank;
+    tb.slot_expert[slot] = id;
+    tb.pair_token[slot] = 0;
+    tb.pair_slot[slot] = slot;
+    tb.pair_gate[slot] = gate;
+    tb.gts[lane] = gate;
+  }
+  for (int sidx = lane; sidx <= S; sidx += 32) tb.slot_begin[sidx] = sidx;
+  if (lane == 0) {
+    if (first) { tb.slot_expert[0] = -1; tb.pair_token[0] = 0; tb.pair_slot[0] = 0; tb.pair_gate[0] = 1.0f; }
+    tb.n_routed = K;
+    tb.n_slots = S;
+    tb.n_pairs = S;
+    tb.shared_slot = first ? 0 : -1;
+  }
+}
+
 __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb, int layer, uint8_t* scratch) {
   const int M = p.M, E = p.E, K = p.K;
   // per-warp candidate buffers live in the gate/up partial-sum region (not live during
@@ -381,13 +448,26 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
       __syncwarp();
     }
   }
+  const int first = p.has_shared ? 1 : 0;
+  if (M == 1) {
+    // one token: warp 0 selected it and builds the tables in registers, no block barrier
+    if (warp == 0) {
+      __syncwarp();
+      if (!tb.bad) routing_tables_one(tb, K, first, lane);
+    }
+    __syncthreads();
+    MDW_TRACE_POINT(layer, 10);
+    MDW_TRACE_POINT(layer, 11);
+    if (tb.bad) return;
+    if (blockIdx.x == 0) publish_routing(p, tb, layer);
+    return;
+  }
   __syncthreads();
   MDW_TRACE_POINT(layer, 10);
   if (tb.bad) return;
   // Routing tables (warp 0): gates, the union of the selections and its slots (slot 0 = shared
   // expert when present, then the union ascending); then the pairs (slot-major,
   // token-minor).
-  const int first = p.has_shared ? 1 : 0;
   auto slot_of = [&](int e) {
     return first + tb.wpre[e >> 5] + __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
   };
@@ -480,27 +560,7 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
       for (int t = lane; t < M; t += 32) { tb.pair_token[t] = t; tb.pair_slot[t] = 0; tb.pair_gate[t] = 1.0f; }
   }
   __syncthreads();
-  if (blockIdx.x == 0) {
-    // publish the routing (inspection + optional outputs)
-    for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
-      p.ids[i] = tb.ids[i];
-      p.gates[i] = tb.gts[i];
-      if (p.ids_out) p.ids_out[i] = tb.ids[i];
-      if (p.gates_out) p.gates_out[i] = tb.gts[i];
-    }
-    for (int s = threadIdx.x; s < tb.n_slots; s += blockDim.x) p.slot_expert[s] = tb.slot_expert[s];
-    for (int q = threadIdx.x; q < tb.n_pairs; q += blockDim.x) {
-      p.pair_token[q] = tb.pair_token[q];
-      p.pair_slot[q] = tb.pair_slot[q];
-      p.pair_gate[q] = tb.pair_gate[q];
-    }
-    if (threadIdx.x == 0) {
-      p.hdr[kHdrSlots] = tb.n_slots;
-      p.hdr[kHdrPairs] = tb.n_pairs;
-      p.hdr[kHdrRouted] = tb.n_routed;
-      if (layer < kHdrWords - kHdrUnions) p.hdr[kHdrUnions + layer] = tb.n_routed;
-    }
-  }
+  if (blockIdx.x == 0) publish_routing(p, tb, layer);
 }
 
 // ------------------------------------------------------------------ P3: gate/up + SwiGLU
