@@ -70,7 +70,7 @@ constexpr int kGuBcStages = 3;
 constexpr int kGuBcStageBytes = 16 * kGuU * 16 + 16 * kGuU;
 constexpr int kWarpRingBc = (kGuBcStages * kGuBcStageBytes > kDnStages * kDnStageBytes)
                                 ? kGuBcStages * kGuBcStageBytes : kDnStages * kDnStageBytes;
-__host__ __device__ constexpr int warp_ring_bytes(int M) { return M <= 2 ? kWarpRingBc : kWarpRing; }
+__host__ __device__ constexpr int warp_ring_bytes(int M) { return M <= 4 ? kWarpRingBc : kWarpRing; }
 constexpr int kMaxRowsPerBlock = 32;            // down-projection rows per block (>= H / grid)
 
 // ------------------------------------------------------------------ phase trace
@@ -595,20 +595,29 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // E8M0 scales in fp32. The MMAs need no per-block fresh accumulator and the weights no
 // scaling, so the step costs about half the instructions of the token-column form.
 //
-// bc_step: wr0 / wr1 = block sb + q of rows g and g + 8; xb = the x-hat (f16, natural order)
-// of token g >> 2 on block sb + q when q == (g & 3), else null. Adds the partial dots of the
-// lane's columns 2q, 2q + 1 (token q >> 1, blocks sb + 2 (q & 1) + {0, 1}) into d.
-__device__ __forceinline__ void bc_step(uint4 wr0, uint4 wr1, const uint8_t* xb, float (&d)[4]) {
+// With three or four tokens a second m16n8 tile (NT = 2) carries tokens 2 and 3 the same way:
+// tile j's column c = token 2j + (c >> 2), block c & 3; both tiles share the converted
+// weights.
+//
+// bc_step: wr0 / wr1 = block sb + q of rows g and g + 8; xb[j] = the x-hat (f16, natural
+// order) of token 2j + (g >> 2) on block sb + q when q == (g & 3), else null. Adds the partial
+// dots of the lane's columns 2q, 2q + 1 of each tile (token 2j + (q >> 1), blocks
+// sb + 2 (q & 1) + {0, 1}) into d[j].
+template <int NT>
+__device__ __forceinline__ void bc_step(uint4 wr0, uint4 wr1, const uint8_t* const (&xb)[NT], float (&d)[NT][4]) {
   const uint32_t A[4] = {wr0.x, wr0.y, wr0.z, wr0.w}, B[4] = {wr1.x, wr1.y, wr1.z, wr1.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint4 xv = make_uint4(0, 0, 0, 0);
-    if (xb) xv = *reinterpret_cast<const uint4*>(xb + 16 * w);
     uint32_t ha[4], hb[4];
     e2m1x8_to_f16x2x4(A[w], ha);
     e2m1x8_to_f16x2x4(B[w], hb);
-    mma_16816(d, ha[0], hb[0], ha[1], hb[1], xv.x, xv.y);
-    mma_16816(d, ha[2], hb[2], ha[3], hb[3], xv.z, xv.w);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      uint4 xv = make_uint4(0, 0, 0, 0);
+      if (xb[j]) xv = *reinterpret_cast<const uint4*>(xb[j] + 16 * w);
+      mma_16816(d[j], ha[0], hb[0], ha[1], hb[1], xv.x, xv.y);
+      mma_16816(d[j], ha[2], hb[2], ha[3], hb[3], xv.z, xv.w);
+    }
   }
 }
 // acc[0] (row g) and acc[1] (row g + 8) += the lane's two columns scaled by the rows' E8M0
@@ -621,20 +630,32 @@ __device__ __forceinline__ void bc_scale_add(const float (&d)[4], uint32_t sa0, 
   acc[1] = fmaf(e8m0_to_f32(sb0), d[2], acc[1]);
   acc[1] = fmaf(e8m0_to_f32(sb1), d[3], acc[1]);
 }
-// End of a block-column unit: the lane pairs (q, q ^ 1) add their blocks, then lane q == 0
-// collects token 1 from lane 2, giving the token-column layout of an m16n8 result:
-// r = {row g token 0, row g token 1, row g+8 token 0, row g+8 token 1} on lane q == 0, zeros
-// on the other lanes (their columns would be tokens >= 2).
-__device__ __forceinline__ void bc_finish(const float (&acc)[2], int q, float (&r)[4]) {
-  const float a0 = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 1);
-  const float a1 = acc[1] + __shfl_xor_sync(0xffffffffu, acc[1], 1);
-  const float t0 = __shfl_xor_sync(0xffffffffu, a0, 2);
-  const float t1 = __shfl_xor_sync(0xffffffffu, a1, 2);
-  const bool own = (q == 0);
-  r[0] = own ? a0 : 0.f;
-  r[1] = own ? t0 : 0.f;
-  r[2] = own ? a1 : 0.f;
-  r[3] = own ? t1 : 0.f;
+// End of a block-column unit: per tile, the lane pairs (q, q ^ 1) add their blocks and lane
+// q == 0 collects the tile's second token from lane 2; tile j's pair of tokens then moves to
+// lane q == j, giving the token-column layout of an m16n8 result:
+// r = {row g token 2q, row g token 2q+1, row g+8 token 2q, row g+8 token 2q+1} on lanes
+// q < NT, zeros on the others.
+template <int NT>
+__device__ __forceinline__ void bc_finish(const float (&acc)[NT][2], int q, float (&r)[4]) {
+  float rr[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const float a0 = acc[j][0] + __shfl_xor_sync(0xffffffffu, acc[j][0], 1);
+    const float a1 = acc[j][1] + __shfl_xor_sync(0xffffffffu, acc[j][1], 1);
+    rr[j][0] = a0;
+    rr[j][1] = __shfl_xor_sync(0xffffffffu, a0, 2);
+    rr[j][2] = a1;
+    rr[j][3] = __shfl_xor_sync(0xffffffffu, a1, 2);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v = (q == 0) ? rr[0][i] : 0.f;
+    if (NT > 1) {
+      const float t = __shfl_up_sync(0xffffffffu, rr[NT > 1 ? 1 : 0][i], 1);
+      if (q == 1) v = t;
+    }
+    r[i] = v;
+  }
 }
 
 // One gate/up unit: MMA rows 0..7 = gate rows j0..j0+7 and rows 8..15 = the matching up rows
@@ -644,6 +665,7 @@ struct GuUnit {
   const uint8_t* q13;
   const uint8_t* s13;
   const uint8_t* xtok;
+  const uint8_t* xtok2;       // block-column form with two tiles: the lane's token of tile 1
   int j0, nr, kb0;
 };
 
@@ -658,8 +680,10 @@ struct GuUnit {
 // accumulators); otherwise each block's fresh fp32 result is scaled in fp32 and added. At the
 // end of unit j, done(j, acc) receives
 //   acc[0..1] = gate rows g, tokens 2q..2q+1;  acc[2..3] = up rows g, same tokens.
-template <bool BC, typename Info, typename Done>
+template <int BCN, typename Info, typename Done>
 __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done done, uint8_t* ring, int lane) {
+  constexpr bool BC = BCN > 0;                 // block-column form with BCN tiles, else token columns
+  constexpr int NT = BC ? BCN : 1;
   constexpr int STAGES = BC ? kGuBcStages : kGuStages;
   constexpr int SBYTES = BC ? kGuBcStageBytes : kGuStageBytes;
   const int g = lane >> 2, q = lane & 3;
@@ -696,7 +720,7 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
     cp_async_commit();
   }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // even / odd blocks
-  float bcacc[2] = {0.f, 0.f};                                       // block columns: rows g, g + 8
+  float bcacc[NT][2] = {};                                           // block columns: tiles x rows g, g + 8
   for (int st = 0; st < total; ++st) {
     if (st + STAGES - 1 < total) issue(st + STAGES - 1);
     cp_async_commit();
@@ -721,16 +745,21 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
           s0 = *reinterpret_cast<const uint16_t*>(scp + g * 8 + sb + 2 * (q & 1));
           s1 = *reinterpret_cast<const uint16_t*>(scp + (g + 8) * 8 + sb + 2 * (q & 1));
         }
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        bc_step(w0, w1, U.xtok ? U.xtok + 64 * (bb + sb + q) : nullptr, d);
-        bc_scale_add(d, s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc);
+        float d[NT][4] = {};
+        const uint8_t* xb[NT];
+        xb[0] = U.xtok ? U.xtok + 64 * (bb + sb + q) : nullptr;
+        if (NT > 1) xb[NT - 1] = U.xtok2 ? U.xtok2 + 64 * (bb + sb + q) : nullptr;
+        bc_step<NT>(w0, w1, xb, d);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) bc_scale_add(d[j], s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc[j]);
       }
       __syncwarp();
       if (st % spu == spu - 1) {
         float r[4];
-        bc_finish(bcacc, q, r);
+        bc_finish<NT>(bcacc, q, r);
         done(st / spu, r);
-        bcacc[0] = bcacc[1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) bcacc[j][0] = bcacc[j][1] = 0.f;
       }
       continue;
     }
@@ -821,6 +850,7 @@ __device__ void build_gate_up_tiles(Tables& tb, int a, int b) {
 
 // All gate/up tiles of the block's list: units (tile, K half) in rounds of kGuRound; the two
 // halves' partials are summed in a fixed order, then SwiGLU, then h per (pair, row).
+template <int MAXM>
 __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, Tables& tb,
                               int trace_layer = kTraceNone) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -839,7 +869,11 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
   }
   const int units = tb.gu_n * ks;
   const int kpart = kHBlocks / ks;
-  const bool bc = p.M <= 2;                        // block-column MMAs (at most two tokens a tile)
+  // MMA form, fixed per kernel instantiation (each carries only its own loop, which keeps the
+  // register allocation of the small-M kernels free of the other forms): block columns with
+  // one tile for up to two tokens, two tiles for up to four, token columns beyond
+  constexpr int BCN = MAXM <= 2 ? 1 : MAXM <= 4 ? 2 : 0;
+  const bool bc = BCN > 0;
   const int round = kGuRound / ks * ks;            // a whole number of tiles per round
   uint8_t* ring = const_cast<uint8_t*>(smem) + smem_layout(p.M).ring + (size_t)warp * warp_ring_bytes(p.M);
   for (int u0 = 0; u0 < units; u0 += round) {
@@ -854,9 +888,12 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
       GuUnit U;
       U.q13 = e < 0 ? L.sh_w13_q : L.w13_q + (size_t)e * kRows13 * kW13RowBytes;
       U.s13 = e < 0 ? L.sh_w13_s : L.w13_s + (size_t)e * kRows13 * kHBlocks;
-      if (bc) {       // lane (g, q) feeds token g >> 2 of the tile, on its own block q == g & 3
+      U.xtok2 = nullptr;
+      if (bc) {       // lane (g, q) feeds token 2j + (g >> 2) of tile j, on its own block q == g & 3
         const int tt = g >> 2;
         U.xtok = (q == (g & 3) && t.w + tt < m) ? smem + (size_t)tb.pair_token[pb + t.w + tt] * kXhBytes : nullptr;
+        U.xtok2 = (q == (g & 3) && t.w + 2 + tt < m) ? smem + (size_t)tb.pair_token[pb + t.w + 2 + tt] * kXhBytes
+                                                     : nullptr;
       } else {
         U.xtok = (t.w + g < m) ? smem + (size_t)tb.pair_token[pb + t.w + g] * kXhBytes : nullptr;
       }
@@ -868,8 +905,7 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
     auto done = [&](int j, const float (&acc)[4]) {
       red[(warp + j * kWarps) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     };
-    if (bc) gate_up_units<true>(mine, 10 / ks, info, done, ring, lane);
-    else gate_up_units<false>(mine, 10 / ks, info, done, ring, lane);
+    gate_up_units<BCN>(mine, 10 / ks, info, done, ring, lane);
     __syncthreads();
     MDW_TRACE_POINT(trace_layer, 16);
     for (int u = warp; u < un; u += kWarps) {
@@ -936,6 +972,31 @@ __device__ void quantise_pairs(const MoeParams& p, uint8_t* smem, Tables& tb, in
 //  * Leftover rows (nrows mod 16) on the CUDA cores, one warp per (slot, row).
 // Every (pair, row) result is multiplied by the pair's gate and h scale into `part`, and the
 // per-token sums are taken in pair order, so the output does not depend on scheduling.
+// One down-projection unit in block-column form (NT tiles): 16 W2 rows x 12 blocks staged in
+// buf (rows of kDnBcPitch bytes, then the rows' 24 scale bytes); h0 / h1 = the lane's h-hat
+// of tile 0 / 1 (or null). Result in the token-column layout (see bc_finish).
+template <int NT>
+__device__ __forceinline__ void down_bc_unit(const uint8_t* buf, int g, int qd, int kb0, const uint8_t* h0,
+                                             const uint8_t* h1, float (&r)[4]) {
+  const uint8_t* scp = buf + 16 * kDnBcPitch;
+  float bcacc[NT][2] = {};
+#pragma unroll
+  for (int sb = 0; sb < kDnKB; sb += 4) {
+    const uint4 w0 = *reinterpret_cast<const uint4*>(buf + g * kDnBcPitch + (sb + qd) * 16);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(buf + (g + 8) * kDnBcPitch + (sb + qd) * 16);
+    const uint32_t s0 = *reinterpret_cast<const uint16_t*>(scp + g * kIBlocks + kb0 + sb + 2 * (qd & 1));
+    const uint32_t s1 = *reinterpret_cast<const uint16_t*>(scp + (g + 8) * kIBlocks + kb0 + sb + 2 * (qd & 1));
+    float d[NT][4] = {};
+    const uint8_t* xb[NT];
+    xb[0] = h0 ? h0 + 64 * (kb0 + sb + qd) : nullptr;
+    if (NT > 1) xb[NT - 1] = h1 ? h1 + 64 * (kb0 + sb + qd) : nullptr;
+    bc_step<NT>(w0, w1, xb, d);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) bc_scale_add(d[j], s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc[j]);
+  }
+  bc_finish<NT>(bcacc, qd, r);
+}
+
 // Down-projection unit list of pairs [q0, q0 + n): (slot, full 16-row tile, K half, 8-pair
 // group). The slots of the chunk (at most kPairChunk + 1, 32 per round of warp 0) and their
 // unit counts (tiles x 8-pair groups x 2 K halves) are scanned; then every thread writes
@@ -988,6 +1049,7 @@ __device__ __forceinline__ int down_full_tiles(int G) {
   return (r1 - r0) / 16;
 }
 
+template <int MAXM>
 __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* smem, Tables& tb,
                              int layer, bool first_list_ready) {
   const int M = p.M, G = gridDim.x;
@@ -1015,7 +1077,8 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     s2 = e < 0 ? L.sh_w2_s : L.w2_s + (size_t)e * kH * kIBlocks;
   };
   const int NP = tb.n_pairs;
-  const bool bc = M <= 2;                          // block-column MMAs (at most two pairs a slot)
+  constexpr int BCN = MAXM <= 2 ? 1 : MAXM <= 4 ? 2 : 0;   // as in gate_up_tiles
+  const bool bc = BCN > 0;
   for (int q0 = 0; q0 < NP; q0 += kPairChunk) {
     const int n = min(kPairChunk, NP - q0);
     __syncthreads();
@@ -1102,23 +1165,14 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
         const int pz = min(tb.slot_begin[t.x + 1], q0 + n);
         const int kb0 = t.z * kDnKB;
         if (bc) {
-          // block columns: lane (g, q) feeds pair t.w + (g >> 2) on its own block q == g & 3
+          // block columns: lane (g, q) feeds pair t.w + 2j + (g >> 2) of tile j on its own block
+          // q == g & 3
           const int tt = g >> 2;
-          const uint8_t* hbc = (qd == (g & 3) && t.w + tt < pz) ? smem + sl.hh + (size_t)(t.w + tt - q0) * kHhBytes : nullptr;
-          const uint8_t* scp = buf + 16 * kDnBcPitch;
-          float bcacc[2] = {0.f, 0.f};
-#pragma unroll
-          for (int sb = 0; sb < kDnKB; sb += 4) {
-            const uint4 w0 = *reinterpret_cast<const uint4*>(buf + g * kDnBcPitch + (sb + qd) * 16);
-            const uint4 w1 = *reinterpret_cast<const uint4*>(buf + (g + 8) * kDnBcPitch + (sb + qd) * 16);
-            const uint32_t s0 = *reinterpret_cast<const uint16_t*>(scp + g * kIBlocks + kb0 + sb + 2 * (qd & 1));
-            const uint32_t s1 = *reinterpret_cast<const uint16_t*>(scp + (g + 8) * kIBlocks + kb0 + sb + 2 * (qd & 1));
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            bc_step(w0, w1, hbc ? hbc + 64 * (kb0 + sb + qd) : nullptr, d);
-            bc_scale_add(d, s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc);
-          }
+          const uint8_t* h0 = (qd == (g & 3) && t.w + tt < pz) ? smem + sl.hh + (size_t)(t.w + tt - q0) * kHhBytes : nullptr;
+          const uint8_t* h1 = (qd == (g & 3) && t.w + 2 + tt < pz) ? smem + sl.hh + (size_t)(t.w + 2 + tt - q0) * kHhBytes
+                                                                   : nullptr;
           float r[4];
-          bc_finish(bcacc, qd, r);
+          down_bc_unit<BCN ? BCN : 1>(buf, g, qd, kb0, h0, h1, r);
           __syncwarp();
           red[(warp + k * kWarps) * 32 + lane] = make_float4(r[0], r[1], r[2], r[3]);
           continue;
@@ -1306,7 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
       MDW_TRACE_POINT(layer, 5);
       build_gate_up_tiles(tb, a, b);
       if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
-      gate_up_tiles(p, L, smem, tb, layer);
+      gate_up_tiles<MAXM>(p, L, smem, tb, layer);
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);
@@ -1317,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
     if (p.stack_mode && layer + 1 < p.L) prefetch_static(p, p.layers[layer + 1]);
     if (!bar.wait()) return;
     MDW_TRACE_POINT(layer, 7);
-    down_combine(p, L, smem, tb, layer, true);
+    down_combine<MAXM>(p, L, smem, tb, layer, true);
     MDW_TRACE_POINT(layer, 8);
     if (p.stack_mode && layer + 1 < p.L) {
       if (!bar.sync()) return;                                      // B3 (r_{l+1})
