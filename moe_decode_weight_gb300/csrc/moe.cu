@@ -940,26 +940,45 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
 // into the workspace for inspection).
 __device__ void quantise_pairs(const MoeParams& p, uint8_t* smem, Tables& tb, int q0, int n) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int k = warp; k < n; k += kWarps) {
-    const int q = q0 + k;
-    const float* hv = p.h + (size_t)q * kI;
-    float v[kI / 32];
-    float am = 0.f;
+  constexpr int J = kI / 128;                     // 16-byte loads per lane per pair (6)
+  // one pair per warp at a time, 16-byte loads
+  for (int k0 = warp; k0 < n; k0 += kWarps) {
+    uint4 v[1][J];
 #pragma unroll
-    for (int i = 0; i < kI / 32; ++i) { v[i] = ld_cg_f32(hv + lane + 32 * i); am = fmaxf(am, fabsf(v[i])); }
-    am = warp_max(am);
-    const float s = am > 0.f ? __fdiv_rn(am, kE4M3Max) : 1.0f;
-    if (lane == 0) tb.sh[k] = s;
-    uint8_t* hh = smem + smem_layout(p.M).hh + (size_t)k * kHhBytes;
+    for (int r = 0; r < 1; ++r) {
+      const int k = k0 + r * kWarps;
+      if (k < n) {
+        const uint4* hv = reinterpret_cast<const uint4*>(p.h + (size_t)(q0 + k) * kI);
 #pragma unroll
-    for (int i = 0; i < kI / 32; ++i) {
-      const int e = lane + 32 * i;
-      const uint32_t code = f32x2_to_e4m3x2(__fdiv_rn(v[i], s), 0.f) & 0xFF;
-      const uint32_t f = e4m3x2_to_f16x2(code);
-      *reinterpret_cast<uint16_t*>(hh + (size_t)e * 2) = (uint16_t)f;
-      if (blockIdx.x == 0) p.hq[(size_t)q * kI + e] = (uint8_t)code;
+        for (int j = 0; j < J; ++j) v[r][j] = ld_cg16(hv + lane + 32 * j);
+      }
     }
-    if (blockIdx.x == 0 && lane == 0) p.sh[q] = s;
+#pragma unroll
+    for (int r = 0; r < 1; ++r) {
+      const int k = k0 + r * kWarps;
+      if (k >= n) break;                            // warp-uniform
+      const int q = q0 + k;
+      float am = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        am = fmaxf(am, fmaxf(fmaxf(fabsf(__uint_as_float(v[r][j].x)), fabsf(__uint_as_float(v[r][j].y))),
+                             fmaxf(fabsf(__uint_as_float(v[r][j].z)), fabsf(__uint_as_float(v[r][j].w)))));
+      am = warp_max(am);
+      const float s = am > 0.f ? __fdiv_rn(am, kE4M3Max) : 1.0f;
+      if (lane == 0) tb.sh[k] = s;
+      uint8_t* hh = smem + smem_layout(p.M).hh + (size_t)k * kHhBytes;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = 4 * (lane + 32 * j);          // elements e .. e + 3
+        const uint32_t c01 = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(v[r][j].x), s),
+                                             __fdiv_rn(__uint_as_float(v[r][j].y), s));
+        const uint32_t c23 = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(v[r][j].z), s),
+                                             __fdiv_rn(__uint_as_float(v[r][j].w), s));
+        *reinterpret_cast<uint2*>(hh + (size_t)e * 2) = make_uint2(e4m3x2_to_f16x2(c01), e4m3x2_to_f16x2(c23));
+        if (blockIdx.x == 0) *reinterpret_cast<uint32_t*>(p.hq + (size_t)q * kI + e) = c01 | (c23 << 16);
+      }
+      if (blockIdx.x == 0 && lane == 0) p.sh[q] = s;
+    }
   }
 }
 
