@@ -298,7 +298,7 @@ def _workload(m: int) -> str:
             f"bf16 pre-norm residual) + online-FP8 LM head 157184x2560 + argmax/top-29, M={m}")
 
 
-def sweep(layers, head, device, ms=(1, 2, 4, 8, 16), steps: int = 3, warmup: int = 3):
+def sweep(layers, head, device, ms=(1, 2, 4, 8, 16, 32), steps: int = 3, warmup: int = 3):
     """The layer stack at several M, with the router's own routing and with Zipf(1.1)-popular
     routing imposed (seed 4 + layer): per M the step time, the mean realised union and the
     achieved GB/s of the stack (algorithmic bytes of the realised unions)."""

@@ -87,7 +87,7 @@ typedef enum mdw_format {
 #define MDW_INTER 768
 #define MDW_MAX_EXPERTS 512
 #define MDW_MAX_TOPK 8
-#define MDW_MAX_M 16
+#define MDW_MAX_M 32
 #define MDW_MAX_VOCAB_TOPK 32
 
 /* Weights of one MoE layer. Fill every field; set magic = MDW_MAGIC and
@@ -191,8 +191,8 @@ mdw_status moe_decode_layer(const mdw_moe_weights* w, int32_t M, const void* x_b
                             float* topk_w_out, void* ws, size_t ws_bytes, mdw_stream_t stream);
 
 /* Bytes of the scratch array that the library holds on every GPU it runs on, for
- * moe_decode_layer_noalloc (1 MiB). */
-#define MDW_NOALLOC_SCRATCH_BYTES (1u << 20)
+ * moe_decode_layer_noalloc (2 MiB). */
+#define MDW_NOALLOC_SCRATCH_BYTES (2u << 20)
 
 /* moe_decode_layer without a caller workspace. The pages have no counterpart: this is an
  * integration entry point of this library.
@@ -241,7 +241,9 @@ size_t mdw_lm_head_workspace_bytes(const mdw_lm_head* head, int32_t M, int32_t t
  * fp32 accumulation. Outputs (device): logits (NULL = not written) fp32 [M][V];
  * argmax_out int32 [M] (required); topk_idx int32 [M][topk] and topk_val fp32 [M][topk]
  * (NULL = not written; topk in 1..MDW_MAX_VOCAB_TOPK), descending, ties -> lower index.
- * head->fmt must be MDW_FMT_FP8_E4M3_ROWSCALE, else MDW_ERR_FORMAT_MISMATCH. */
+ * head->fmt must be MDW_FMT_FP8_E4M3_ROWSCALE, else MDW_ERR_FORMAT_MISMATCH.
+ * Tokens are independent here: a window of more than 16 tokens runs as launches of up to 16
+ * tokens each, every launch streaming the head once (1 <= M <= MDW_MAX_M). */
 mdw_status lm_head_fp8(const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
                        int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val,
                        void* ws, size_t ws_bytes, mdw_stream_t stream);

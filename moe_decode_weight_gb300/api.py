@@ -23,7 +23,7 @@ STATUS = {0: "MDW_OK", 1: "MDW_ERR_INVALID_ARG", 2: "MDW_ERR_UNSUPPORTED_SHAPE",
           3: "MDW_ERR_FORMAT_MISMATCH", 4: "MDW_ERR_WORKSPACE_TOO_SMALL", 5: "MDW_ERR_CUDA",
           6: "MDW_ERR_TIMEOUT", 7: "MDW_ERR_DEVICE_BOUNDS"}
 HIDDEN, INTER = 2560, 768
-MAX_M, MAX_TOPK, MAX_VOCAB_TOPK, MAX_EXPERTS = 16, 8, 32, 512
+MAX_M, MAX_TOPK, MAX_VOCAB_TOPK, MAX_EXPERTS = 32, 8, 32, 512
 
 # exported symbols declared in include/moe_decode_weight.h
 SYMBOLS = ["mdw_status_string", "mdw_version", "mdw_moe_workspace_bytes", "mdw_moe_workspace_layout",

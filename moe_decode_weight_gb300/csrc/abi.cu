@@ -42,7 +42,7 @@ MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk) {
   l.hq = take(P * kI);
   l.sh = take(P * 4);
   w.resid = stack ? take((size_t)2 * M * kH * 2) : 0;
-  w.cand = stack ? take(head_ws_bytes(M, topk, head_grid())) : 0;
+  w.cand = stack ? take(head_ws_bytes(M < 16 ? M : 16, topk, head_grid())) : 0;   // one 16-token head launch
   l.total = o;
   w.total = o;
   return w;
@@ -119,30 +119,45 @@ struct Draw {                     // optional draw on the final top-k
   int32_t* out = nullptr;
 };
 
+// Tokens per head launch: the head kernels are instantiated for up to 16 tokens; a larger
+// window runs as consecutive launches on the same stream (tokens are independent in the head,
+// and each launch streams the head once).
+constexpr int kHeadChunkM = 16;
+int head_chunk_m(int M) { return M < kHeadChunkM ? M : kHeadChunkM; }
+
 mdw_status head_call(const mdw_lm_head* head, int fmt, int32_t M, const void* h_bf16, int norm_input,
                      float* logits, int32_t* argmax_out, int32_t topk, int32_t* topk_idx,
                      float* topk_val, uint32_t* hdr, uint8_t* cand, cudaStream_t s, const Draw& draw = Draw()) {
-  HeadParams hp{};
-  hp.sample_u = draw.u;
-  hp.temperature = draw.temperature;
-  hp.top_p = draw.top_p;
-  hp.sample_out = draw.out;
-  hp.w = static_cast<const uint8_t*>(head->w);
-  hp.row_scale = head->row_scale;
-  hp.V = head->vocab;
-  hp.M = M;
-  hp.topk = topk;
-  hp.x = static_cast<const __nv_bfloat16*>(h_bf16);
-  hp.norm_input = norm_input;
-  hp.logits = logits;
-  hp.argmax_out = argmax_out;
-  hp.topk_idx = topk_idx;
-  hp.topk_val = topk_val;
-  hp.hdr = hdr;
-  const size_t n = (size_t)(head_grid() + kHeadMaxGroups) * M * topk;
-  hp.cand_val = reinterpret_cast<float*>(cand);
-  hp.cand_idx = reinterpret_cast<int32_t*>(cand + align_up(n * 4, 256));
-  return cuda_status(fmt == MDW_FMT_FP8_E4M3_ROWSCALE ? launch_head_fp8(hp, s) : launch_head_bf16(hp, s));
+  const size_t n = (size_t)(head_grid() + kHeadMaxGroups) * head_chunk_m(M) * topk;
+  for (int t0 = 0; t0 < M; t0 += kHeadChunkM) {
+    // later launches: the previous launch's merge counters back to zero (the status word stays)
+    if (t0 > 0 && (cudaMemsetAsync(hdr + kHdrDoneCtr, 0, 4, s) != cudaSuccess ||
+                   cudaMemsetAsync(hdr + kHdrHeadGroups, 0, kHeadMaxGroups * 4, s) != cudaSuccess))
+      return MDW_ERR_CUDA;
+    HeadParams hp{};
+    hp.sample_u = draw.u ? draw.u + t0 : nullptr;
+    hp.temperature = draw.temperature;
+    hp.top_p = draw.top_p;
+    hp.sample_out = draw.out ? draw.out + t0 : nullptr;
+    hp.w = static_cast<const uint8_t*>(head->w);
+    hp.row_scale = head->row_scale;
+    hp.V = head->vocab;
+    hp.M = M - t0 < kHeadChunkM ? M - t0 : kHeadChunkM;
+    hp.topk = topk;
+    hp.x = static_cast<const __nv_bfloat16*>(h_bf16) + (size_t)t0 * kH;
+    hp.norm_input = norm_input;
+    hp.logits = logits ? logits + (size_t)t0 * head->vocab : nullptr;
+    hp.argmax_out = argmax_out ? argmax_out + t0 : nullptr;
+    hp.topk_idx = topk_idx ? topk_idx + (size_t)t0 * topk : nullptr;
+    hp.topk_val = topk_val ? topk_val + (size_t)t0 * topk : nullptr;
+    hp.hdr = hdr;
+    hp.cand_val = reinterpret_cast<float*>(cand);
+    hp.cand_idx = reinterpret_cast<int32_t*>(cand + align_up(n * 4, 256));
+    const mdw_status st =
+        cuda_status(fmt == MDW_FMT_FP8_E4M3_ROWSCALE ? launch_head_fp8(hp, s) : launch_head_bf16(hp, s));
+    if (st != MDW_OK) return st;
+  }
+  return MDW_OK;
 }
 
 mdw_status head_entry(int fmt, const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
@@ -266,7 +281,7 @@ size_t mdw_lm_head_workspace_bytes(const mdw_lm_head* head, int32_t M, int32_t t
   if (!head || M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK) return 0;
   const int g = head_grid();
   if (g <= 0) return 0;
-  const size_t n = (size_t)(g + kHeadMaxGroups) * M * topk;     // block lists + group lists
+  const size_t n = (size_t)(g + kHeadMaxGroups) * head_chunk_m(M) * topk;   // block + group lists
   return kHdrWords * 4 + align_up(n * 4, 256) + align_up(n * 4, 256);
 }
 

@@ -45,6 +45,8 @@ constexpr int kRows13 = 2 * kI;                 // w13 rows per expert
 constexpr int kW13RowBytes = kH / 2;            // 1280
 constexpr int kW2RowBytes = kI / 2;             // 384
 constexpr int kXhBytes = kH * 2 + 64;           // f16 x-hat per token, padded (conflict-free B loads)
+constexpr int kXh8Bytes = kH + 32;              // E4M3 x-hat per token (M > 16), padded likewise
+constexpr int kTablesBytes = 18432;             // shared memory reserved for the per-block tables
 constexpr int kGuRound = 4 * kWarps;            // gate/up units per round (partials in smem)
 constexpr int kGuMaxTiles = 320;                // (tile, token-tile) entries per block
 constexpr int kMaxSegs = 48;                    // slot segments per block list (>= kPairChunk + 1)
@@ -100,21 +102,31 @@ struct Smem {
   size_t xh, xb, hh, ring, part, yacc, gured, small, total;
 };
 // R1 = x-hat (gate/up) or h-hat (down); R2 = bf16 x (router) or the per-warp cp.async rings.
+// Up to 16 tokens the x-hat is f16; beyond, it is kept as E4M3 codes (decoded to f16 at the
+// fragment loads) and the router's bf16 x spans R1 and R2 until the codes replace it.
 __host__ __device__ inline Smem smem_layout(int M) {
   Smem s;
-  const size_t r1 = (size_t)M * kXhBytes > (size_t)kPairChunk * kHhBytes ? (size_t)M * kXhBytes
-                                                                          : (size_t)kPairChunk * kHhBytes;
   const size_t rings = (size_t)kWarps * warp_ring_bytes(M);
-  const size_t r2 = (size_t)M * kH * 2 > rings ? (size_t)M * kH * 2 : rings;
+  const size_t hh = (size_t)kPairChunk * kHhBytes;
   s.xh = 0;
   s.hh = 0;
-  s.xb = (r1 + 127) & ~(size_t)127;
-  s.ring = s.xb;
-  s.part = (s.xb + r2 + 15) & ~(size_t)15;                      // [kPairChunk][rows] fp32
+  if (M > 16) {
+    const size_t r1 = (size_t)M * kXh8Bytes > hh ? (size_t)M * kXh8Bytes : hh;
+    s.xb = 0;
+    s.ring = (r1 + 127) & ~(size_t)127;
+    const size_t end = s.ring + rings > (size_t)M * kH * 2 ? s.ring + rings : (size_t)M * kH * 2;
+    s.part = (end + 15) & ~(size_t)15;
+  } else {
+    const size_t r1 = (size_t)M * kXhBytes > hh ? (size_t)M * kXhBytes : hh;
+    const size_t r2 = (size_t)M * kH * 2 > rings ? (size_t)M * kH * 2 : rings;
+    s.xb = (r1 + 127) & ~(size_t)127;
+    s.ring = s.xb;
+    s.part = (s.xb + r2 + 15) & ~(size_t)15;                    // [kPairChunk][rows] fp32
+  }
   s.yacc = s.part + (size_t)kPairChunk * kMaxRowsPerBlock * 4;     // [M][rows] fp32
   s.gured = s.yacc + (size_t)M * kMaxRowsPerBlock * 4;               // [kGuRound][32][4] fp32
   s.small = s.gured + (size_t)kGuRound * 32 * 4 * 4;   // also holds the routing candidates
-  s.total = s.small + 12288;
+  s.total = s.small + kTablesBytes;
   return s;
 }
 
@@ -141,7 +153,7 @@ struct Tables {
   int seg_slot[kMaxSegs], seg_lo[kMaxSegs], seg_hi[kMaxSegs], seg_groups[kMaxSegs], seg_off[kMaxSegs + 1];
   int4 gu_tile[kGuMaxTiles];                   // (slot, j0, rows, first token column)
 };
-static_assert(sizeof(Tables) <= 12288, "tables exceed the reserved shared memory");
+static_assert(sizeof(Tables) <= kTablesBytes, "tables exceed the reserved shared memory");
 
 // ------------------------------------------------------------------ P0: input / act quant
 
@@ -216,6 +228,7 @@ __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tabl
     if (blockIdx.x == 0) p.sx[threadIdx.x] = sc;
   }
   __syncthreads();
+  if (MAXM > 16) return;                          // codes written after the router (xhat_codes_in_place)
   const bool writer = (blockIdx.x == 0);
   for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
     const int t = c / CPT, i = c % CPT;           // chunk i = elements 8i .. 8i+7 of token t
@@ -232,6 +245,48 @@ __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tabl
     *reinterpret_cast<uint4*>(smem + (size_t)t * kXhBytes + (size_t)i * 16) = make_uint4(h[0], h[1], h[2], h[3]);
     if (writer)
       reinterpret_cast<uint2*>(p.xq + (size_t)t * kH)[i] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+  }
+  __syncthreads();
+}
+
+// E4M3 x-hat of more than 16 tokens, once the router has read the bf16 x: token t's codes
+// (the same quotients and rounding as above) move from its bf16 row at byte t * 2H to byte
+// t * kXh8Bytes. Groups of 6 tokens, 5 chunks per thread: a group's rows are all read into
+// registers before any of its codes is written, and a group's codes end below the first byte
+// of the next group's rows, so no row is overwritten before it is read.
+__device__ void xhat_codes_in_place(const MoeParams& p, uint8_t* smem, const Tables& tb) {
+  constexpr int CPT = kH / 8;                     // 8-value chunks per token
+  constexpr int GT = 6;                           // tokens per group
+  constexpr int CH = GT * CPT / kThreads;         // chunks per thread per group
+  static_assert(GT * CPT % kThreads == 0, "a group must give every thread the same chunk count");
+  static_assert(kXh8Bytes <= 2 * kH, "codes must not pass the rows they replace");
+  const int M = p.M;
+  const uint4* xb4 = reinterpret_cast<const uint4*>(smem + smem_layout(M).xb);
+  const bool writer = (blockIdx.x == 0);
+  for (int t0 = 0; t0 < M; t0 += GT) {
+    uint4 v[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int c = t0 * CPT + (int)threadIdx.x + j * kThreads;
+      v[j] = c < M * CPT ? xb4[c] : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int c = t0 * CPT + (int)threadIdx.x + j * kThreads;
+      if (c >= M * CPT) continue;
+      const int t = c / CPT, i = c % CPT;
+      const float sc = tb.sx[t];
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      uint32_t q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        q[k] = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[k] << 16), sc),
+                               __fdiv_rn(__uint_as_float(w[k] & 0xFFFF0000u), sc));
+      const uint2 codes = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+      *reinterpret_cast<uint2*>(smem + smem_layout(M).xh + (size_t)t * kXh8Bytes + (size_t)i * 8) = codes;
+      if (writer) reinterpret_cast<uint2*>(p.xq + (size_t)t * kH)[i] = codes;
+    }
   }
   __syncthreads();
 }
@@ -680,7 +735,7 @@ struct GuUnit {
 // accumulators); otherwise each block's fresh fp32 result is scaled in fp32 and added. At the
 // end of unit j, done(j, acc) receives
 //   acc[0..1] = gate rows g, tokens 2q..2q+1;  acc[2..3] = up rows g, same tokens.
-template <int BCN, typename Info, typename Done>
+template <int BCN, bool X8, typename Info, typename Done>
 __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done done, uint8_t* ring, int lane) {
   constexpr bool BC = BCN > 0;                 // block-column form with BCN tiles, else token columns
   constexpr int NT = BC ? BCN : 1;
@@ -780,7 +835,15 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
         wu = *reinterpret_cast<const uint32_t*>(buf + (g + 8) * kGuPitch + u * 16 + 4 * q);
       }
       uint4 xv = make_uint4(0, 0, 0, 0);
-      if (U.xtok) xv = *reinterpret_cast<const uint4*>(U.xtok + 64 * (bb + u) + 16 * q);
+      if (U.xtok) {
+        if (X8) {                                      // E4M3 codes 8q..8q+7 of the block -> f16
+          const uint2 c = *reinterpret_cast<const uint2*>(U.xtok + 32 * (bb + u) + 8 * q);
+          xv = make_uint4(e4m3x2_to_f16x2(c.x & 0xFFFFu), e4m3x2_to_f16x2(c.x >> 16), e4m3x2_to_f16x2(c.y & 0xFFFFu),
+                          e4m3x2_to_f16x2(c.y >> 16));
+        } else {
+          xv = *reinterpret_cast<const uint4*>(U.xtok + 64 * (bb + u) + 16 * q);
+        }
+      }
       const uint32_t sgb = ((u < 4 ? scg.x : scg.y) >> (8 * (u & 3))) & 0xFF;
       const uint32_t sub = ((u < 4 ? scu.x : scu.y) >> (8 * (u & 3))) & 0xFF;
       uint32_t hg[4], hu[4];
@@ -895,7 +958,8 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
         U.xtok2 = (q == (g & 3) && t.w + 2 + tt < m) ? smem + (size_t)tb.pair_token[pb + t.w + 2 + tt] * kXhBytes
                                                      : nullptr;
       } else {
-        U.xtok = (t.w + g < m) ? smem + (size_t)tb.pair_token[pb + t.w + g] * kXhBytes : nullptr;
+        constexpr size_t xs = MAXM > 16 ? kXh8Bytes : kXhBytes;
+        U.xtok = (t.w + g < m) ? smem + (size_t)tb.pair_token[pb + t.w + g] * xs : nullptr;
       }
       U.j0 = t.y;
       U.nr = t.z;
@@ -905,7 +969,7 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
     auto done = [&](int j, const float (&acc)[4]) {
       red[(warp + j * kWarps) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     };
-    gate_up_units<BCN>(mine, 10 / ks, info, done, ring, lane);
+    gate_up_units<BCN, (MAXM > 16)>(mine, 10 / ks, info, done, ring, lane);
     __syncthreads();
     MDW_TRACE_POINT(trace_layer, 16);
     for (int u = warp; u < un; u += kWarps) {
@@ -1362,6 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
       router_rows(p, L, smem, wv);
     }
     bar.arrive();                                                   // B1 (logits)
+    if (MAXM > 16) xhat_codes_in_place(p, smem, tb);                 // the router is done with x
     MDW_TRACE_POINT(layer, 2);
     MDW_TRACE_POINT(layer, 3);
     if (!bar.wait()) return;
@@ -1377,9 +1442,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
       const int a = 8 * (int)((long long)blockIdx.x * T / G), b = 8 * (int)((long long)(blockIdx.x + 1) * T / G);
       MDW_TRACE_POINT(layer, 12);
       MDW_TRACE_POINT(layer, 5);
-      build_gate_up_tiles(tb, a, b);
-      if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
-      gate_up_tiles<MAXM>(p, L, smem, tb, layer);
+      if (MAXM <= 16) {
+        // one list (a share of up to 16 tokens' tiles always fits)
+        build_gate_up_tiles(tb, a, b);
+        if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
+        gate_up_tiles<MAXM>(p, L, smem, tb, layer);
+      } else {
+        // in pieces whose tile list always fits: a 32-token window with a large union can put
+        // many tiles of four 8-token column groups into one share (a loop here in the smaller
+        // kernels measured 3 % slower at M = 4, so they keep the single list)
+        constexpr int kPiece = 8 * (kGuMaxTiles / ((MAXM + 7) / 8));
+        for (int a0 = a; a0 < b; a0 += kPiece) {
+          build_gate_up_tiles(tb, a0, min(b, a0 + kPiece));
+          if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
+          gate_up_tiles<MAXM>(p, L, smem, tb, layer);
+        }
+      }
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);
@@ -1424,7 +1502,8 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s) {
   if (p.M <= 2) return launch_t<2>(p, s);
   if (p.M <= 4) return launch_t<4>(p, s);
   if (p.M <= 8) return launch_t<8>(p, s);
-  return launch_t<16>(p, s);
+  if (p.M <= 16) return launch_t<16>(p, s);
+  return launch_t<32>(p, s);
 }
 
 }  // namespace mdw

@@ -15,7 +15,7 @@
 namespace mdw {
 namespace {
 
-// The scratch of every moe_decode_layer_noalloc call on this GPU. 1 MiB holds the
+// The scratch of every moe_decode_layer_noalloc call on this GPU. 2 MiB hold the
 // workspace of any call moe_decode_layer accepts (M <= MDW_MAX_M, E <= 512, top_k <= 8).
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MDW_NOALLOC_SCRATCH_BYTES];
 

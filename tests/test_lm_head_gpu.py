@@ -75,7 +75,7 @@ def _run_head(fn, head, h, V, k, with_logits=True):
             lg.cpu().numpy() if lg is not None else None)
 
 
-@pytest.mark.parametrize("m", [1, 4, 16])
+@pytest.mark.parametrize("m", [1, 4, 16, 32])
 @pytest.mark.parametrize("V,k", [(20011, 29), (1000, 29), (5003, 1), (5003, 32)])
 def test_lm_head_fp8_parity(m, V, k):
     w = _weight(V, specials=False)

@@ -49,9 +49,11 @@ def run_layer(layer, x, y_fp32=True, residual=None, override=None):
     return dict(y=y, ws=ws, ids=ids.cpu().numpy(), gates=gw.cpu().numpy(), status=status)
 
 
-def check_layer(layer, x, out, override=None):
-    """Full step-by-step parity of one call; returns the end-to-end max relative error."""
+def check_layer(layer, x, out, override=None, tokens=None):
+    """Full step-by-step parity of one call; returns the teacher-forced y. Codes, routing, union
+    and pairs are checked for every token; h, hq and y for the given tokens (default: all)."""
     m = x.shape[0]
+    tokens = set(range(m)) if tokens is None else set(tokens)
     K = layer.K
     assert out["status"] == 0
     ws = out["ws"]
@@ -96,6 +98,8 @@ def check_layer(layer, x, out, override=None):
     y_tf = np.zeros((m, H))
     for q in range(P):
         t, e = int(ptok[q]), int(slots[pslot[q]])
+        if t not in tokens:
+            continue
         w13q, w13s, w2q, w2s = layer.expert(e) if e >= 0 else layer.shared()
         gate, up = OM.expert_gate_up(w13q, w13s, xq_o[t], sx_o[t])
         h_o = OM.swiglu(gate, up)
@@ -124,6 +128,36 @@ def test_layer_parity_512(layer512, m):
     frac_ok = bar_ok(y, y_e2e).mean()
     assert frac_ok > 0.99, f"end-to-end y within the bar for only {frac_ok:.4f} of outputs"
     assert np.max(np.abs(y - y_e2e)) < 2e-2 * np.sqrt(np.mean(y_e2e ** 2))
+
+
+def test_layer_parity_512_m32(layer512):
+    """A 32-token window: the x-hat is kept as E4M3 codes in shared memory (converted in place
+    from the router's bf16 rows in groups of 6 tokens) and each block's gate/up share runs in
+    pieces. Codes, routing, union and pairs are checked for all 32 tokens; h and the teacher-
+    forced y for tokens on both sides of conversion-group edges (5 | 6, 17 | 18) and in the
+    short last group (30, 31)."""
+    m = 32
+    x = hidden_with_gap(42, m, layer512.wr, layer512.K)
+    out = run_layer(layer512, x)
+    toks = [0, 5, 6, 17, 18, 30, 31]
+    y_tf = check_layer(layer512, x, out, tokens=toks)
+    y = out["y"].cpu().numpy()
+    assert np.isfinite(y).all()
+    assert_bar(y[toks], y_tf[toks], "y (teacher-forced hq), M=32")
+
+
+def test_layer_m32_zipf_override(layer512):
+    """32 tokens under Zipf(1.1) popularity: popular experts carry many tokens, so their tiles
+    have up to four 8-token column groups."""
+    m = 32
+    x = hidden_with_gap(43, m, layer512.wr, layer512.K)
+    ov = synth.zipf_topk(44, m, num_experts=512, top_k=8)
+    out = run_layer(layer512, x, override=torch.from_numpy(ov))
+    toks = [0, 11, 31]
+    y_tf = check_layer(layer512, x, out, override=ov, tokens=toks)
+    y = out["y"].cpu().numpy()
+    assert np.isfinite(y).all()
+    assert_bar(y[toks], y_tf[toks], "y (teacher-forced hq), M=32 Zipf")
 
 
 def test_layer_small_no_shared_topk4(layer64):

@@ -17,6 +17,12 @@ pytestmark = pytest.mark.gpu
 H = 2560
 
 
+def _nucleus_margin(vals, temperature, top_p):
+    """The u-independent part of the decision margin: how far the nucleus cut is from moving
+    (a uniform outside [0, 1) leaves only those terms of the oracle's margin)."""
+    return OS.decision_margin(vals, temperature, top_p, 2.0)
+
+
 def _uniforms(vals, temperature, top_p, seed, margin):
     rng = np.random.default_rng(seed)
     out = []
@@ -56,7 +62,7 @@ def test_sample_topk_rejects_bad_settings():
             api.mdw_sample_topk(v, i, 0.6, tp, u, o)
 
 
-@pytest.mark.parametrize("m", [1, 4])
+@pytest.mark.parametrize("m", [1, 4, 20])
 def test_head_fused_draw(m):
     """FP8 head + draw in one launch; the oracle draws from its own float64 top-29."""
     V, k, T, P = 20011, 29, 0.6, 0.95
@@ -71,12 +77,15 @@ def test_head_fused_draw(m):
         for attempt in range(100):
             h = synth.hidden_states(7000 + t, 1, attempt)
             lg = OL.lm_head_fp8_logits(qo, so, bf16_to_np(h))
-            if topk_gap_ok(lg, k):
-                rows.append(h)
-                ii = OL.topk(lg, k)
-                vv = np.take_along_axis(lg, ii, axis=1)
-                tops.append((vv[0], ii[0]))
-                break
+            if not topk_gap_ok(lg, k):
+                continue
+            ii = OL.topk(lg, k)
+            vv = np.take_along_axis(lg, ii, axis=1)
+            if _nucleus_margin(vv[0], T, P) <= 1e-3:     # no uniform could make this draw clean
+                continue
+            rows.append(h)
+            tops.append((vv[0], ii[0]))
+            break
         else:
             raise RuntimeError("no hidden state with clean gaps")
     x = torch.cat(rows, 0).cuda()

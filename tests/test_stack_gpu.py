@@ -120,3 +120,39 @@ def test_stack_imposed_routing_bounds(model):
     api.moe_decode_stack_routed([l.weights for l in layers], None, synth.hidden_states(5, m, 0).cuda(), None,
                                 ws, torch.from_numpy(ov).cuda(), resid_out=resid)
     assert api.mdw_device_status(ws) == 7
+
+
+def test_stack_m32_imposed_routing_with_head(model):
+    """A 32-token window through the stack and the FP8 head (which runs as two 16-token
+    launches): every layer teacher-forced on tokens 0, 6 and 31 (tokens are independent), the
+    head's logits and top-k checked for all 32 tokens."""
+    layers, head, (qo, so), V = model
+    L, m, k = len(layers), 32, 29
+    ov = np.stack([synth.zipf_topk(40 + l, m, num_experts=64, top_k=8) for l in range(L)])
+    r0 = synth.hidden_states(6, m, 0)
+    ws = torch.zeros(api.mdw_stack_workspace_bytes([l.weights for l in layers], head, m, k),
+                     dtype=torch.uint8, device="cuda")
+    resid = torch.zeros((L + 1, m, H), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((m,), -1, dtype=torch.int32, device="cuda")
+    ti = torch.full((m, k), -1, dtype=torch.int32, device="cuda")
+    lg = torch.zeros((m, V), dtype=torch.float32, device="cuda")
+    api.moe_decode_stack_routed([l.weights for l in layers], head, r0.cuda(), am, ws,
+                                torch.from_numpy(ov).cuda(), resid_out=resid, logits=lg, topk=k, topk_idx=ti)
+    assert api.mdw_device_status(ws) == 0
+    hdr = ws[:1024].cpu().numpy().view(np.uint32)
+    rs = resid.float().cpu().numpy()
+    toks = [0, 6, 31]
+    for l, layer in enumerate(layers):
+        assert int(hdr[64 + l]) == len(set(ov[l].reshape(-1).tolist()))
+        r_next, _, res = OS.layer_step(rs[l][toks], layer.oracle_dict(), layer.K, topk_override=ov[l][toks])
+        _check_residual(rs[l + 1][toks], r_next, res["y"], f"layer {l}")
+    lo = OL.lm_head_fp8_logits(qo, so, OS.rmsnorm_bf16(rs[L]))
+    assert np.max(np.abs(lg.cpu().numpy() - lo)) < 1e-2
+    tin, amn = ti.cpu().numpy(), am.cpu().numpy()
+    for t in range(m):
+        order = np.lexsort((np.arange(V), -lo[t]))
+        clean = -np.diff(lo[t, order[:k + 1]]) > 1e-3
+        n = k if clean.all() else int(np.argmin(clean))
+        assert np.array_equal(tin[t, :n], order[:n]), f"token {t}"
+        if clean[0]:
+            assert amn[t] == order[0]
