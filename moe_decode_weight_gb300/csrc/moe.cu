@@ -911,6 +911,52 @@ __device__ void build_gate_up_tiles(Tables& tb, int a, int b) {
   __syncthreads();
 }
 
+// Tile list of the kernels for more than 8 tokens, where a slot can have several 8-token
+// column groups: the work space is every (slot, tile of 8 row pairs, column group) entry,
+// slot-major, then tile, then group (slot s has 96 ceil(m_s / 8) entries), and the block takes
+// entries [E b / G, E (b + 1) / G) of the E in all. Shares of whole tiles would give the
+// blocks holding the shared expert's tiles (M tokens: ceil(M / 8) groups per tile) several
+// times the work of the others. A share holds at most (257 slots x 96 + 36 x 96) / 152 < 190
+// entries. `scratch` (n_slots + 1 ints) holds the slots' entry offsets. Every thread of the
+// block must call it.
+__device__ void build_gate_up_entries(Tables& tb, int* scratch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = tb.n_slots, G = gridDim.x;
+  constexpr int kTilesPerSlot = kI / 8;
+  if (warp == 0) {
+    int carry = 0;
+    for (int b0 = 0; b0 < S; b0 += 32) {
+      const int sidx = b0 + lane;
+      const int c = sidx < S ? kTilesPerSlot * ((tb.slot_begin[sidx + 1] - tb.slot_begin[sidx] + 7) / 8) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      if (sidx < S) scratch[sidx] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) scratch[S] = carry;
+  }
+  __syncthreads();
+  const long long E = scratch[S];
+  const int e0 = (int)(E * blockIdx.x / G), e1 = (int)(E * (blockIdx.x + 1) / G);
+  const int n = e1 - e0 < kGuMaxTiles ? e1 - e0 : kGuMaxTiles;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = e0 + i;
+    int lo = 0, hi = S - 1;                 // the slot with scratch[s] <= e < scratch[s + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (scratch[mid] <= e) lo = mid; else hi = mid - 1;
+    }
+    const int gq = (tb.slot_begin[lo + 1] - tb.slot_begin[lo] + 7) / 8, local = e - scratch[lo];
+    tb.gu_tile[i] = make_int4(lo, 8 * (local / gq), 8, 8 * (local % gq));
+  }
+  if (threadIdx.x == 0) tb.gu_n = e1 - e0 > kGuMaxTiles ? -1 : e1 - e0;   // -1: does not fit
+  __syncthreads();
+}
+
 // All gate/up tiles of the block's list: units (tile, K half) in rounds of kGuRound; the two
 // halves' partials are summed in a fixed order, then SwiGLU, then h per (pair, row).
 template <int MAXM>
@@ -1436,28 +1482,21 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
     if (tb.bad) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
     {
       // gate/up tiles of 8 row pairs of every slot (the shared expert is slot 0; 96 whole
-      // tiles per slot), dealt to the blocks in equal contiguous shares of whole tiles, so no
-      // block pays for a tile cut at a share boundary
+      // tiles per slot), dealt to the blocks in equal contiguous shares of whole tiles (up to
+      // 8 tokens) or of (tile, column group) entries (more tokens), so no block pays for a
+      // tile cut at a share boundary
       const long long T = (long long)tb.n_slots * (kI / 8);
       const int a = 8 * (int)((long long)blockIdx.x * T / G), b = 8 * (int)((long long)(blockIdx.x + 1) * T / G);
       MDW_TRACE_POINT(layer, 12);
       MDW_TRACE_POINT(layer, 5);
-      if (MAXM <= 16) {
-        // one list (a share of up to 16 tokens' tiles always fits)
+      if (MAXM <= 8) {
+        // up to 8 tokens every slot has one column group: equal shares of whole tiles
         build_gate_up_tiles(tb, a, b);
-        if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
-        gate_up_tiles<MAXM>(p, L, smem, tb, layer);
       } else {
-        // in pieces whose tile list always fits: a 32-token window with a large union can put
-        // many tiles of four 8-token column groups into one share (a loop here in the smaller
-        // kernels measured 3 % slower at M = 4, so they keep the single list)
-        constexpr int kPiece = 8 * (kGuMaxTiles / ((MAXM + 7) / 8));
-        for (int a0 = a; a0 < b; a0 += kPiece) {
-          build_gate_up_tiles(tb, a0, min(b, a0 + kPiece));
-          if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
-          gate_up_tiles<MAXM>(p, L, smem, tb, layer);
-        }
+        build_gate_up_entries(tb, reinterpret_cast<int*>(smem + smem_layout(p.M).gured));
       }
+      if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
+      gate_up_tiles<MAXM>(p, L, smem, tb, layer);
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);
