@@ -392,6 +392,22 @@ def moe_traffic(layers: int, m: int):
         return None
 
 
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The largest of every rank's x (the slowest replica sets the job's time); x itself when
+    the job has one rank."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def per_token_us(total_ms: float, steps: int, m: int, world: int) -> float:
+    """Whole-job µs per token: every rank decodes m tokens per step, so a step of the job
+    yields m x world tokens in the time of its slowest rank."""
+    return total_ms / steps * 1000.0 / (m * world)
+
+
 def run_gpu(args, rank: int, world: int):
     from moe_decode_weight_gb300 import api
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -406,13 +422,9 @@ def run_gpu(args, rank: int, world: int):
     clocks = ClockSampler(local).start()
     res = time_steps(st, args.steps, args.warmup, dist_barrier)
     clk = clocks.stop()
-    total_ms = res["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(res["total_ms"], device, world)
     ms_step = total_ms / args.steps
-    us_token = ms_step * 1000.0 / (args.m * world)
+    us_token = per_token_us(total_ms, args.steps, args.m, world)
     lay_ms = float(np.mean(res["layer_ms"]))
     head_ms = float(np.mean(res["head_ms"]))
     b_lay = float(np.mean(res["bytes_layers"]))
@@ -422,10 +434,7 @@ def run_gpu(args, rank: int, world: int):
     step_gbs = b_step / (ms_step * 1e6)
 
     e2e_ms, h2d, d2h = time_e2e(st, args.steps, args.warmup)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, device, world)
 
     extra = {}
     if not args.no_m4 and args.m == 1:
@@ -477,7 +486,7 @@ def run_gpu(args, rank: int, world: int):
                      "kernel": "moe_persistent_kernel (42 layers, one launch)",
                      "peak_kind": peak_kind},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_ms * 1000.0 / (args.steps * args.m * world), "unit": "us/token",
+        "e2e": {"value": per_token_us(e2e_ms, args.steps, args.m, world), "unit": "us/token",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,

@@ -124,3 +124,25 @@ def test_stack_rejects_mixed_layers():
                                 FAKE, 1 << 30, None) == 3
     assert lib.moe_decode_stack(layers, 0, C.byref(head), 1, FAKE, None, None, FAKE, 1, None, None,
                                 FAKE, 1 << 30, None) == 1
+
+
+def _define(name):
+    m = re.search(r"#define\s+" + name + r"\s+\(?(\d+)u?(?:\s*<<\s*(\d+))?\)?", open(HEADER).read())
+    assert m, name
+    return int(m.group(1)) << int(m.group(2) or 0)
+
+
+def test_binding_limits_match_the_header():
+    assert api.MAX_M == _define("MDW_MAX_M")
+    assert api.MAX_TOPK == _define("MDW_MAX_TOPK")
+    assert api.MAX_VOCAB_TOPK == _define("MDW_MAX_VOCAB_TOPK")
+    assert api.MAX_EXPERTS == _define("MDW_MAX_EXPERTS")
+
+
+def test_noalloc_scratch_holds_the_largest_layer_workspace():
+    """moe_decode_layer_noalloc must accept every shape moe_decode_layer accepts: the workspace
+    of the largest window (M = MDW_MAX_M, 512 experts, top-8) fits the compiled-in scratch."""
+    lib = api.lib()
+    w = _weights()
+    biggest = lib.mdw_moe_workspace_bytes(C.byref(w), api.MAX_M)
+    assert 0 < biggest <= _define("MDW_NOALLOC_SCRATCH_BYTES")
