@@ -375,17 +375,27 @@ def time_sampler(head, st, device, steps: int = 20):
     return out
 
 
+def kernel_code_digest(paths) -> str:
+    """sha256 of the kernel sources with comments and blank lines removed: it changes with
+    any change to the code and not with documentation edits."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in paths:
+        text = open(os.path.join(ROOT, f)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(l.rstrip() for l in text.splitlines() if l.strip()).encode())
+    return h.hexdigest()
+
+
 def moe_traffic(layers: int, m: int):
     """DRAM bytes (read + write) of one stack launch from the committed ncu capture, scaled
-    by the layer count; None unless the kernel sources still hash to the captured ones and
-    the bench runs the captured M."""
-    import hashlib
+    by the layer count; None unless the kernel code still matches the captured code and the
+    bench runs the captured M."""
     try:
         meta = json.load(open(os.path.join(ROOT, "profiles", "moe_traffic.json")))
-        h = hashlib.sha256()
-        for f in meta["sources"]:
-            h.update(open(os.path.join(ROOT, f), "rb").read())
-        if h.hexdigest() != meta["sources_sha256"] or m != 1:
+        if kernel_code_digest(meta["sources"]) != meta["code_sha256"] or m != 1:
             return None
         return float(meta["dram_bytes_per_layer_m1"]) * layers
     except (OSError, KeyError, ValueError):

@@ -22,18 +22,19 @@
 //       input, so no exchange is needed;
 //   P1  router logits for its slice of the E router rows -> global; B1;
 //   P2  top-k + dedup redundantly from the E x M logits (every block derives the same slot /
-//       pair tables; slot 0 is the shared expert); as soon as the slots are known, warps
-//       1.. issue bulk L2 prefetches of every weight byte the block reads in the layer
-//       while warp 0 finishes the pair tables;
-//   P3  gate/up for its contiguous share of the (slot, row-pair) space -> h; arrive(B2);
-//       (stack) L2 prefetch of the next layer's static weights; wait(B2);
+//       pair tables; slot 0 is the shared expert);
+//   P3  gate/up for its contiguous share of the (slot, row-pair tile) space -- of the
+//       (slot, tile, 8-token column group) space above 8 tokens -> h; arrive(B2); while
+//       waiting: bulk L2 prefetch of its W2 rows of every slot and (stack) of the next
+//       layer's router rows and shared-expert slice; wait(B2);
 //   P4  every block quantises all pairs' h (amax / 448) into shared memory, then computes
 //       its slice of output rows over all slots (no atomics: a fixed summation order);
 //       (stack) r_{l+1} = bf16(r_l + y); B3.
-//   The expert GEMVs run on m16n8k16 tensor-core MMAs: with at most two tokens the MMA
-//   columns carry (token, K-block) pairs (block-column form, scales applied per column in
-//   fp32); with more tokens they carry tokens, the E8M0 scale folded into the f16 weights
-//   when that is exact (token-column form).
+//   The expert GEMVs run on m16n8k16 tensor-core MMAs: with up to four tokens the MMA
+//   columns carry (token, K-block) pairs (block-column form, one or two tiles, scales applied
+//   per column in fp32); with more tokens they carry tokens, the E8M0 scale folded into the
+//   f16 weights when that is exact (token-column form); above 16 tokens the expert input is
+//   kept in shared memory as E4M3 codes and widened to f16 at the fragment loads.
 // Every inter-block wait is bounded and records MDW_ERR_TIMEOUT instead of hanging.
 #include "mdw_device.cuh"
 #include "mdw_internal.h"
