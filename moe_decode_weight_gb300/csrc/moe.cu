@@ -66,9 +66,9 @@ constexpr int kDnBcPitch = kDnKB * 16;          // 192 bytes (= 64 mod 128): con
 constexpr int kDnStageBytes = 16 * kDnPitch + 16 * kIBlocks;
 constexpr int kWarpRing = (kGuStages * kGuStageBytes > kDnStages * kDnStageBytes)
                               ? kGuStages * kGuStageBytes : kDnStages * kDnStageBytes;
-// block-column form (M <= 2): unpadded 128-byte rows (swizzled chunks); the same depth as
-// the token-column ring (a deeper ring measured slower: more requests in flight per SM
-// delayed the first stages)
+// block-column form (M <= 4): unpadded 128-byte rows (swizzled chunks); the same depth as
+// the token-column ring (4 or 5 stages measured no faster at M = 1 and 2-4 % slower at
+// M = 2 and 4: the phase is not limited by the bytes a warp has in flight)
 constexpr int kGuBcStages = 3;
 constexpr int kGuBcStageBytes = 16 * kGuU * 16 + 16 * kGuU;
 constexpr int kWarpRingBc = (kGuBcStages * kGuBcStageBytes > kDnStages * kDnStageBytes)
@@ -730,7 +730,8 @@ struct GuUnit {
 // the fragment reads are bank-conflict free), the next unit's stages being requested while
 // the current one is computed. Each 32-block is two k16 MMAs on a permuted K order: lane
 // (g, q) feeds bytes 4q..4q+3 of the block (E2M1 pairs, via cvt.e2m1x2) as its A registers
-// and the matching x-hat values 8q..8q+7 (one 16-byte load) as its B registers. When every
+// and the matching x-hat values 8q..8q+7 (one 16-byte load of f16 values, or above 16 tokens
+// one 8-byte load of E4M3 codes widened to f16) as its B registers. When every
 // E8M0 scale of a stage keeps E2M1 x 2^(s-127) exact in f16, the scale is multiplied into the
 // f16 weights and the MMAs accumulate straight into fp32 (even and odd blocks in two
 // accumulators); otherwise each block's fresh fp32 result is scaled in fp32 and added. At the
@@ -1099,7 +1100,7 @@ __device__ void quantise_pairs(const MoeParams& p, uint8_t* smem, Tables& tb, in
 //    B = h-hat of up to 8 of the slot's tokens (f16), K = 768 split in two halves of 12
 //    blocks (one unit each, staged through the warp's cp.async ring); each block's fresh
 //    result is scaled by the row's E8M0 scale in fp32; the halves are added in a fixed order.
-//  * Leftover rows (nrows mod 16) on the CUDA cores, one warp per (slot, row).
+//  * Leftover rows (nrows mod 16) on the CUDA cores, one warp per (pair, row).
 // Every (pair, row) result is multiplied by the pair's gate and h scale into `part`, and the
 // per-token sums are taken in pair order, so the output does not depend on scheduling.
 // One down-projection unit in block-column form (NT tiles): 16 W2 rows x 12 blocks staged in
