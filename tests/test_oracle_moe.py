@@ -134,6 +134,18 @@ def test_combine_closed_form_with_shared():
         assert np.allclose(res["y"][t], base[t] * c, rtol=1e-10, atol=1e-9)
 
 
+def test_zero_routed_experts_leave_the_shared_expert():
+    """Routed experts whose codes are all zero (E2M1 0 = +0, any scale) contribute exactly
+    nothing, so y is the shared expert's dense MLP alone (gate 1), whatever the routing."""
+    (w1, w3, w2), packed, x = _dense_mlp_case(seed=12, m=3)
+    q13, s13, q2, s2 = packed
+    zero = (np.zeros_like(q13), s13, np.zeros_like(q2), s2)
+    wr = np.random.default_rng(13).standard_normal((E, H)).astype(np.float32) * 0.02
+    res = OM.moe_layer(x, wr, lambda e: zero, packed, top_k=4)
+    assert np.allclose(res["y"], _dense_expected(w1, w3, w2, x), rtol=1e-10, atol=1e-9)
+    assert len(res["union"]) >= 4
+
+
 def test_topk_override_uses_given_ids():
     (w1, w3, w2), packed, x = _dense_mlp_case(seed=10, m=2)
     wr = np.random.default_rng(1).standard_normal((E, H)).astype(np.float32) * 0.02
