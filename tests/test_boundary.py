@@ -146,3 +146,21 @@ def test_noalloc_scratch_holds_the_largest_layer_workspace():
     w = _weights()
     biggest = lib.mdw_moe_workspace_bytes(C.byref(w), api.MAX_M)
     assert 0 < biggest <= _define("MDW_NOALLOC_SCRATCH_BYTES")
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 8, 16, 17, 31, 32])
+def test_workspace_regions_hold_their_arrays(m):
+    """Every region of the moe_decode_layer workspace holds the array the header documents
+    for M tokens (P = M (top_k + 1) pairs, S = M top_k + 1 slots), for every window size."""
+    lib = api.lib()
+    w = _weights()
+    lay = api.MoeWsLayoutC()
+    assert lib.mdw_moe_workspace_layout(C.byref(w), m, C.byref(lay)) == 0
+    E, K, H, I = 512, 8, 2560, 768
+    P, S = m * (K + 1), m * K + 1
+    need = {"header": 256 * 4, "xq": m * H, "sx": m * 4, "logits": m * E * 4, "ids": m * K * 4,
+            "gates": m * K * 4, "slot_expert": S * 4, "pair_token": P * 4, "pair_slot": P * 4,
+            "pair_gate": P * 4, "h": P * I * 4, "hq": P * I, "sh": P * 4}
+    names = [n for n, _ in api.MoeWsLayoutC._fields_]
+    for a, b in zip(names, names[1:]):
+        assert getattr(lay, b) - getattr(lay, a) >= need[a], a
