@@ -1,5 +1,5 @@
 // Online-FP8 LM head: one-time row-wise quantisation, and the weight-streaming GEMV with a
-// fused arg-max / top-k (block-local lists, then a global merge in the last block).
+// fused arg-max / top-k (block-local lists, merged per group of blocks, then globally).
 //
 // Method: "Three MoE Inference Optimizations NVIDIA Measured on DGX Spark", section
 // "Online FP8 quantization halves the LM head weight reads" -- the BF16 head (157,184 x
@@ -13,7 +13,9 @@
 // MMAs (rows x tokens, fp32 accumulation; FP8 weights converted exactly to f16 in
 // registers), the per-row scale applied once per logit; each warp keeps its running top-k
 // per token in registers (lane i holds the i-th best), the block merges its warps' lists,
-// and the last block to finish merges all blocks' lists.
+// the last block of each group of 16 to finish merges the group's lists, and the last group
+// merges the group lists (and, when asked, draws the token from the final list). A window of
+// more than 16 tokens is several launches (the host side splits it).
 #include "mdw_device.cuh"
 #include "mdw_internal.h"
 #include "mdw_sampler.cuh"
