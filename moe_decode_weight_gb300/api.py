@@ -250,7 +250,8 @@ def mdw_sample_topk(topk_val: torch.Tensor, topk_idx: torch.Tensor, temperature:
 def lm_head_fp8_sample(head: LMHead, h: torch.Tensor, token_out: torch.Tensor, ws: torch.Tensor, u: torch.Tensor,
                        temperature: float, top_p: float, topk: int, norm_input: bool = False, topk_idx=None,
                        topk_val=None, stream=None) -> None:
-    """FP8 head (optionally on bf16(RMSNorm(h))) and the draw on its top-k, in one launch."""
+    """FP8 head (optionally on bf16(RMSNorm(h))) and the draw on its top-k, in one launch per
+    16 tokens."""
     _check("lm_head_fp8_sample",
            lib().lm_head_fp8_sample(C.byref(head.c), h.shape[0], _ptr(h), 1 if norm_input else 0, topk,
                                     float(temperature), float(top_p), _ptr(u), _ptr(token_out), _ptr(topk_idx),
