@@ -18,6 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmdw.so")
+TRACE_LIB = os.path.join(PKG, "libmdw_trace.so")     # profiling build (-DMDW_TRACE), never loaded by the API
 SOURCES = ["moe.cu", "lm_head.cu", "abi.cu", "noalloc.cu", "sampler.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -32,29 +33,32 @@ def nvcc() -> str:
     return path
 
 
-def _compile(src: str) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, trace: bool = False) -> str:
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + (".trace.o" if trace else ".o"))
+    cmd = [nvcc(), *ARCH, *FLAGS, *(["-DMDW_TRACE"] if trace else []), "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    """Build libmdw.so (always rebuilds); returns its path."""
+def build(verbose: bool = False, trace: bool = False) -> str:
+    """Build libmdw.so (always rebuilds); returns its path. trace=True builds the profiling
+    library libmdw_trace.so instead: the same kernels with %globaltimer stamps at their phase
+    boundaries (read by moe_decode_weight_gb300.phase_trace); the product library is untouched."""
     os.makedirs(BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(_compile, SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda src: _compile(src, trace), SOURCES))
+    out = TRACE_LIB if trace else LIB
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {out}")
+    return out
 
 
 if __name__ == "__main__":

@@ -1,0 +1,117 @@
+"""Per-layer phase timeline of the MoE stack kernel, from the profiling build.
+
+``build(trace=True)`` compiles the same kernels with ``-DMDW_TRACE``. Thread 0 of every block
+then writes ``%globaltimer`` at fixed points of every layer into a device table
+(``mdw_trace_read``). This module runs the stack on synthetic weights (seed 3, the bench's
+weights) with that library and prints, per layer, the median and the maximum over blocks of
+each phase. A phase runs from the previous point in kernel order to its own point.
+
+Points inside loops (gate/up rounds, pair chunks) keep their last value, so those phases
+cover the last round / chunk, and "earlier rounds" / "earlier chunks" hold the rest.
+A one-token window builds its routing tables inside the top-k, so "tables" is ~0 there.
+
+    python -m moe_decode_weight_gb300.phase_trace --layers 8 --m 1
+
+The product library ``libmdw.so`` is neither rebuilt nor loaded.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import os
+
+import numpy as np
+
+TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 20, 256   # the device table's shape
+
+# (point id, name of the phase that ends there), in kernel order; point 0 starts a layer
+PHASES = [
+    (1, "input"),                # r -> bf16 x (stack: RMSNorm) -> E4M3 x-hat
+    (2, "router+arrive"),        # router rows, arrival at the logits barrier (M > 16: x-hat codes)
+    (4, "B1 wait"),
+    (10, "top-k"),
+    (11, "tables"),
+    (5, "gate/up list"),
+    (15, "gate/up earlier rounds"),
+    (16, "gate/up last round"),
+    (6, "SwiGLU+arrive"),
+    (7, "B2 wait"),              # W2 prefetch and the first down unit list run in the wait
+    (17, "down earlier chunks"),
+    (18, "h quantisation"),
+    (13, "down unit list"),
+    (19, "down units"),
+    (14, "leftover rows+sum"),
+    (8, "output"),
+    (9, "B3"),
+]
+
+
+def summarise(tr: np.ndarray):
+    """tr: [layers][TRACE_POINTS][blocks] nanosecond stamps. Returns one dict per layer:
+    {"total_us": first start to last B3 exit, phase name: (median_us, max_us) over blocks}."""
+    out = []
+    for lay in tr.astype(np.float64):
+        row = {"total_us": float((lay[9].max() - lay[0].min()) / 1000.0)}
+        prev = 0
+        for point, name in PHASES:
+            d = (lay[point] - lay[prev]) / 1000.0
+            row[name] = (float(np.median(d)), float(d.max()))
+            prev = point
+        out.append(row)
+    return out
+
+
+def format_rows(rows) -> str:
+    lines = ["per layer: phase median / max over blocks (us), from the previous point"]
+    for l, row in enumerate(rows):
+        parts = [f"{name} {row[name][0]:.2f}/{row[name][1]:.2f}" for _, name in PHASES]
+        lines.append(f"L{l}: total {row['total_us']:.2f} | " + " | ".join(parts))
+    return "\n".join(lines)
+
+
+def main() -> None:
+    import torch
+
+    from moe_decode_weight_gb300 import api, build, synth
+
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--runs", type=int, default=4, help="stack launches; the last one is reported")
+    args = ap.parse_args()
+    L, M = args.layers, args.m
+    if not 1 <= L <= TRACE_LAYERS:
+        raise SystemExit(f"--layers must be 1..{TRACE_LAYERS}")
+    api.LIB_PATH = build.build(trace=True)
+    api._lib = None
+    dev = torch.device("cuda:0")
+    layers = []
+    for l in range(L):
+        (w13q, w13s, w2q, w2s), sh = synth.layer_experts(3, l, synth.NUM_EXPERTS, device=dev)
+        wr = synth.router_weight(3, l, synth.NUM_EXPERTS).to(dev)
+        layers.append(api.MoeWeights(wr, w13q, w13s, w2q, w2s, tuple(sh), synth.TOP_K))
+    arr = api._layer_array(layers)
+    ws = torch.zeros(api.mdw_stack_workspace_bytes(layers, None, M, 1), dtype=torch.uint8, device=dev)
+    resid = torch.zeros((L + 1, M, synth.HIDDEN), dtype=torch.bfloat16, device=dev)
+    for it in range(args.runs):
+        r0 = synth.hidden_states(3, M, 100 + it).to(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.moe_decode_stack(arr, None, r0, None, ws, resid_out=resid)
+        e1.record()
+        torch.cuda.synchronize()
+        print(f"run {it}: {e0.elapsed_time(e1) * 1000.0:.1f} us, status {api.mdw_device_status(ws)}")
+    lib = api.lib()
+    lib.mdw_trace_read.argtypes = [C.c_void_p, C.c_size_t]
+    buf = np.zeros(TRACE_LAYERS * TRACE_POINTS * TRACE_BLOCKS, dtype=np.uint64)
+    if lib.mdw_trace_read(buf.ctypes.data, buf.nbytes) != 0:
+        raise SystemExit("mdw_trace_read failed")
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    tr = buf.reshape(TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS)[:L, :, :G]
+    print(f"M = {M}, {L} layers, {G} blocks")
+    print(format_rows(summarise(tr)))
+
+
+if __name__ == "__main__":
+    main()
