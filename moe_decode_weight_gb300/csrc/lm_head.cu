@@ -27,8 +27,9 @@ constexpr int kHeadThreads = kThreads;
 constexpr int kMaxTK = 32;               // list length (lane-distributed; tk <= 32)
 // Built only with -DMDW_TRACE (a profiling build, never the product build): %globaltimer at
 // the head kernel's phase boundaries, per block ([0] start, [1] hidden states ready, [2] all
-// tiles done, [3] block list written, [4] group merge starts, [5] final merge starts, [6]
-// end) and per warp ([8 + warp] its last unit done).
+// tiles done, [20] cut tiles finished, [21] warp lists stored, [22] block tree merged, [3]
+// block list written, [4] group merge starts, [5] final merge starts, [6] end) and per warp
+// ([8 + warp] its last unit done).
 #ifdef MDW_TRACE
 __device__ unsigned long long g_head_trace[kMaxHeadGrid * 24];
 __device__ __forceinline__ void head_trace(int slot) {
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
     *rec_at(warp, 1, nt) = make_float4(part1[nt][0], part1[nt][1], part1[nt][2], part1[nt][3]);
   }
   __syncthreads();
-  MDW_HEAD_TRACE(threadIdx.x == 0, 16);
+  MDW_HEAD_TRACE(threadIdx.x == 0, 20);
   if (nonempty && tL * NG >= u0 && (tL + 1) * NG > u1) {
     float d[NT][4];
 #pragma unroll
@@ -560,7 +561,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
     }
 #ifdef MDW_TRACE
   __syncthreads();
-  MDW_HEAD_TRACE(threadIdx.x == 0, 17);
+  MDW_HEAD_TRACE(threadIdx.x == 0, 21);
   if (threadIdx.x == 0) {
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   }
 #endif
   tree_merge(lv, li, M, warp, lane);
-  MDW_HEAD_TRACE(threadIdx.x == 0, 18);
+  MDW_HEAD_TRACE(threadIdx.x == 0, 22);
   for (int t = warp; t < M; t += kWarps)
     if (lane < tk) {
       const size_t o = ((size_t)blockIdx.x * M + t) * tk + lane;
