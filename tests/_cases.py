@@ -13,7 +13,6 @@ import numpy as np
 import torch
 
 from moe_decode_weight_gb300 import api, synth
-from oracle import formats as F
 from oracle import moe as OM
 
 GAP = 1e-3

@@ -19,7 +19,7 @@ from moe_decode_weight_gb300 import api, synth
 from oracle import formats as F
 from oracle import moe as OM
 
-from _cases import GAP, Layer, assert_bar, bar_ok, bf16_to_np, hidden_with_gap, read_ws, router_gap_ok
+from _cases import Layer, assert_bar, bar_ok, bf16_to_np, hidden_with_gap, read_ws, router_gap_ok
 
 pytestmark = pytest.mark.gpu
 H, I = 2560, 768

@@ -8,13 +8,12 @@ oracle and check that a pin catches it.
 """
 
 import numpy as np
-import pytest
 from scipy.special import expit, softmax
 
 import oracle.moe as OM
 from oracle import formats as F
 
-from _mx_helpers import E2M1_TABLE, pack, random_mx_matrix
+from _mx_helpers import pack, random_mx_matrix
 
 H, I, E = 256, 64, 16
 
