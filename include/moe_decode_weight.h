@@ -154,6 +154,15 @@ const char* mdw_status_string(mdw_status s);
 /* Library version (major*10000 + minor*100 + patch). */
 int32_t mdw_version(void);
 
+/* Test hook, not part of the decode path (the pages have no counterpart). Every inter-block
+ * wait of the MoE kernels is bounded: after `cycles` clock64 cycles (default 1e9, ~0.5 s)
+ * it records MDW_ERR_TIMEOUT in the workspace status word, and every block then leaves the
+ * kernel at its next wait, so a launch always completes. This sets the bound for the calls
+ * enqueued after it, process-wide (cycles <= 0 restores the default) and returns the
+ * previous value. A test makes the bound tiny to check that a wait that runs out ends in
+ * MDW_ERR_TIMEOUT with a usable device context, without faulting or hanging the GPU. */
+int64_t mdw_debug_set_spin_budget(int64_t cycles);
+
 /* Workspace bytes for moe_decode_layer with M tokens; 0 if the arguments are invalid. */
 size_t mdw_moe_workspace_bytes(const mdw_moe_weights* w, int32_t M);
 
@@ -209,7 +218,8 @@ mdw_status moe_decode_layer(const mdw_moe_weights* w, int32_t M, const void* x_b
  * Nothing is allocated: no cudaMalloc / cudaFree, no allocating library routine, no host
  * heap. The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture. Every call on a device shares the one array and re-zeroes the part that must
+ * capture. The address is kept for the life of the process: a cudaDeviceReset() after
+ * the first call on that device is not supported. Every call on a device shares the one array and re-zeroes the part that must
  * start at zero; the array keeps the last call's intermediates otherwise. Calls whose work
  * overlaps on the GPU (different streams without ordering) race on the array.
  *

@@ -31,7 +31,7 @@ SYMBOLS = ["mdw_status_string", "mdw_version", "mdw_moe_workspace_bytes", "mdw_m
            "mdw_lm_head_workspace_bytes", "lm_head_fp8", "lm_head_bf16", "lm_head_fp8_rmsnorm",
            "mdw_stack_workspace_bytes",
            "moe_decode_stack", "mdw_device_status", "moe_decode_layer_noalloc", "mdw_sample_topk",
-           "lm_head_fp8_sample", "moe_decode_stack_routed"]
+           "lm_head_fp8_sample", "moe_decode_stack_routed", "mdw_debug_set_spin_budget"]
 
 
 class MdwError(RuntimeError):
@@ -75,6 +75,8 @@ def lib() -> C.CDLL:
     L.mdw_status_string.restype = C.c_char_p
     L.mdw_status_string.argtypes = [C.c_int]
     L.mdw_version.restype = i32
+    L.mdw_debug_set_spin_budget.restype = i64
+    L.mdw_debug_set_spin_budget.argtypes = [i64]
     L.mdw_moe_workspace_bytes.restype = sz
     L.mdw_moe_workspace_bytes.argtypes = [C.POINTER(MoeWeightsC), i32]
     L.mdw_moe_workspace_layout.restype = C.c_int
@@ -161,6 +163,12 @@ def mdw_status_string(code: int) -> str:
 
 def mdw_version() -> int:
     return lib().mdw_version()
+
+
+def mdw_debug_set_spin_budget(cycles: int) -> int:
+    """Test hook: bound of the kernels' inter-block waits in clock64 cycles (<= 0: the
+    default); returns the previous bound."""
+    return lib().mdw_debug_set_spin_budget(int(cycles))
 
 
 def mdw_moe_workspace_bytes(w: MoeWeights, m: int) -> int:

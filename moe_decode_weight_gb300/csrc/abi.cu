@@ -4,6 +4,7 @@
 // Measured on DGX Spark", section "One missing interface makes the stack slower than
 // baseline": quantisation state travels with the weight handle (magic + format tag), and
 // a handle of the wrong format is an error at the call, never a silent reinterpretation.
+#include <atomic>
 #include <cstring>
 
 #include "mdw_device.cuh"
@@ -18,6 +19,9 @@ int device_sm_count() {
   return n;
 }
 int moe_grid() { return device_sm_count(); }
+
+static std::atomic<long long> g_spin_budget{kSpinBudget};
+long long mdw_spin_budget() { return g_spin_budget.load(std::memory_order_relaxed); }
 int head_grid() { const int n = device_sm_count(); return n > kMaxHeadGrid ? kMaxHeadGrid : n; }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -194,7 +198,12 @@ const char* mdw_status_string(mdw_status s) {
   return "MDW_ERR_UNKNOWN";
 }
 
-int32_t mdw_version(void) { return 100; }
+int32_t mdw_version(void) { return 200; }
+
+int64_t mdw_debug_set_spin_budget(int64_t cycles) {
+  const long long v = cycles > 0 ? (long long)cycles : kSpinBudget;
+  return (int64_t)g_spin_budget.exchange(v);
+}
 
 size_t mdw_moe_workspace_bytes(const mdw_moe_weights* w, int32_t M) {
   if (check_weights(w) != MDW_OK || M < 1 || M > MDW_MAX_M) return 0;
@@ -228,6 +237,7 @@ mdw_status moe_decode_layer(const mdw_moe_weights* w, int32_t M, const void* x_b
   p->L = 1; p->M = M; p->E = w->num_experts; p->K = w->top_k;
   p->has_shared = w->sh_w13_q != nullptr;
   p->stack_mode = 0;
+  p->spin_budget = mdw_spin_budget();
   p->x_in = static_cast<const __nv_bfloat16*>(x_bf16);
   p->y_out = y;
   p->y_fp32 = y_is_fp32 != 0;
@@ -384,6 +394,7 @@ mdw_status moe_decode_stack_routed(const mdw_moe_weights* layers, int32_t L, con
   p->L = L; p->M = M; p->E = E; p->K = K;
   p->has_shared = layers[0].sh_w13_q != nullptr;
   p->stack_mode = 1;
+  p->spin_budget = mdw_spin_budget();
   p->topk_override = topk_override;
   p->r0 = static_cast<const __nv_bfloat16*>(r0_bf16);
   if (resid_out) {

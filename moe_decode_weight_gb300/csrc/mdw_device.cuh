@@ -212,7 +212,7 @@ __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
   return v;
 }
 
-// Bounded spin budget of one barrier wait, in clock64 cycles (~0.5 s at 2 GHz).
+// Default spin budget of one inter-block wait, in clock64 cycles (~0.5 s at 2 GHz).
 constexpr long long kSpinBudget = 1000000000LL;
 
 // Grid-wide barrier over a monotonically increasing arrival counter (zeroed by the host
@@ -223,6 +223,7 @@ constexpr long long kSpinBudget = 1000000000LL;
 struct GridBarrier {
   uint32_t* hdr;
   uint32_t seq;
+  long long budget;             // clock64 cycles one wait may spin before it gives up
   __device__ void arrive() {
     __syncthreads();
     if (threadIdx.x == 0) red_release_add(hdr + kHdrBarrier, 1u);
@@ -237,7 +238,7 @@ struct GridBarrier {
       long long t0 = clock64();
       while ((int)(ld_acquire(hdr + kHdrBarrier) - target) < 0) {
         if (ld_volatile_u32(hdr + kHdrStatus) != 0) { good = 0; break; }
-        if (clock64() - t0 > kSpinBudget) { set_status(hdr, MDW_ERR_TIMEOUT); good = 0; break; }
+        if (clock64() - t0 > budget) { set_status(hdr, MDW_ERR_TIMEOUT); good = 0; break; }
       }
       ok = good;
     }

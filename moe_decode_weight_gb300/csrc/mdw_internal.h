@@ -35,6 +35,7 @@ struct MoeParams {
   int L, M, E, K;              // layers, tokens, routed experts, experts per token
   int has_shared;
   int stack_mode;              // 1: pre-norm residual stack over L layers
+  long long spin_budget;       // clock64 cycles an inter-block wait may spin (mdw_spin_budget())
   // layer mode (L == 1)
   const __nv_bfloat16* x_in;   // [M][H]
   void* y_out;                 // [M][H] fp32 or bf16
@@ -98,6 +99,10 @@ struct MoeWs {
 };
 MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk);
 size_t head_ws_bytes(int M, int topk, int grid);
+
+// Spin budget of the kernels' bounded inter-block waits (the default, or the value set by
+// mdw_debug_set_spin_budget).
+long long mdw_spin_budget();
 
 int device_sm_count();
 int moe_grid();                // co-resident blocks of the MoE kernel (<= SM count)

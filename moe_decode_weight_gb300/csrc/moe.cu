@@ -88,7 +88,7 @@ constexpr int kTraceLayers = 64;
 __device__ unsigned long long g_trace[kTraceLayers * kTracePhases * 256];
 #define MDW_TRACE_POINT(layer, phase)                                                        \
   do {                                                                                       \
-    if (threadIdx.x == 0 && (layer) >= 0 && (layer) < kTraceLayers) {                                        \
+    if (threadIdx.x == 0 && (layer) >= 0 && (layer) < kTraceLayers && blockIdx.x < 256) {                    \
       unsigned long long t_;                                                                 \
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                 \
       g_trace[((layer) * kTracePhases + (phase)) * 256 + blockIdx.x] = t_;                   \
@@ -1458,7 +1458,7 @@ template <int MAXM>
 __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __grid_constant__ MoeParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   Tables& tb = *reinterpret_cast<Tables*>(smem + smem_layout(p.M).small);
-  GridBarrier bar{p.hdr, 0};
+  GridBarrier bar{p.hdr, 0, p.spin_budget};
   const int G = gridDim.x;
   for (int layer = 0; layer < p.L; ++layer) {
     const LayerDesc& L = p.layers[layer];

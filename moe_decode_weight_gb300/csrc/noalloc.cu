@@ -79,6 +79,7 @@ extern "C" mdw_status moe_decode_layer_noalloc(const mdw_moe_weights* w, int32_t
   p.L = 1; p.M = M; p.E = w->num_experts; p.K = w->top_k;
   p.has_shared = w->sh_w13_q != nullptr;
   p.stack_mode = 0;
+  p.spin_budget = mdw_spin_budget();
   p.x_in = static_cast<const __nv_bfloat16*>(x_bf16);
   p.y_out = y;
   p.y_fp32 = y_is_fp32 != 0;

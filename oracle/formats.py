@@ -144,18 +144,3 @@ def quantize_fp8_lastdim(v):
                      np.float32(1.0)).astype(np.float32)
     t = (v32 / scale[..., None]).astype(np.float32)
     return float_to_e4m3_rne_sat(t), scale
-
-
-def e4m3_tie_margin(v, scale) -> np.ndarray:
-    """Relative distance of float32(v)/scale from the nearest E4M3 rounding boundary.
-
-    Used to flag elements whose code may legitimately differ between two computations
-    of v that agree only to float32 rounding (the SwiGLU output is computed in float32
-    on the device and in float64 here).
-    """
-    t = np.abs(np.asarray(v, dtype=np.float64) / np.asarray(scale, dtype=np.float64)[..., None])
-    _, ex = np.frexp(np.where(t > 0, t, 1.0))
-    q = np.where(t >= 2.0 ** -6, np.ldexp(1.0, ex - 1 - 3), 2.0 ** -9)
-    frac = t / q - np.floor(t / q)
-    dist = np.abs(frac - 0.5) * q
-    return dist / np.maximum(t, 2.0 ** -9)

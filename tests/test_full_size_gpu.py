@@ -6,7 +6,7 @@ samples the oracle computes in seconds:
 
 * teacher-forced layers 0, 20 and 41: the oracle's layer fed the device's r_l must give the
   device's r_{l+1};
-* the head's logits of bf16(RMSNorm(r_42)) on 2,000 sampled vocabulary rows;
+* the head's logits of bf16(RMSNorm(r_42)) on 20,000 sampled vocabulary rows, at the bar;
 * the fused top-29 and argmax against a full sort of the kernel's own logits (a property
   that holds at any size).
 """
@@ -19,7 +19,7 @@ from moe_decode_weight_gb300 import api, synth
 from oracle import lm_head as OL
 from oracle import stack as OS
 
-from _cases import Layer, bf16_to_np
+from _cases import Layer, assert_bar, bf16_to_np, norm_rounding_allowance
 from test_stack_gpu import _check_residual
 
 pytestmark = pytest.mark.gpu
@@ -59,14 +59,15 @@ def test_full_step_sampled(full_model, m):
     for l in (0, 20, L - 1):
         r_next, _, res = OS.layer_step(rs[l], layers[l].oracle_dict(), K)
         _check_residual(rs[l + 1], r_next, res["y"], f"layer {l}")
-    # the head on sampled rows of the final residual (the device normalises in fp32, the oracle
-    # in float64, so an input element may sit one bf16 step apart: absolute bound, as in the
-    # stack test)
+    # the head on sampled rows of the final residual, at the bar (the device normalises in
+    # fp32, the oracle in float64: an input element whose bf16 rounding sits at a tie may land
+    # one step apart, which the oracle-derived allowance bounds)
     xf = OS.rmsnorm_bf16(rs[L])
-    rows = np.unique(np.concatenate([[0, V - 1], np.random.default_rng(1).integers(0, V, 2000)]))
+    rows = np.unique(np.concatenate([[0, V - 1], np.random.default_rng(1).integers(0, V, 20000)]))
     qo, so = OL.quantize_lm_head(bf16_to_np(w[torch.from_numpy(rows)]))
     lgn = lg.cpu().numpy()
-    assert np.max(np.abs(lgn[:, rows] - OL.lm_head_fp8_logits(qo, so, xf))) < 1e-2
+    allow = norm_rounding_allowance(rs[L], qo, so)
+    assert_bar(lgn[:, rows], OL.lm_head_fp8_logits(qo, so, xf), "sampled head logits", extra=allow)
     own = np.stack([np.lexsort((np.arange(V), -lgn[t]))[:TOPK] for t in range(m)])
     assert np.array_equal(ti.cpu().numpy(), own)
     assert np.array_equal(am.cpu().numpy(), own[:, 0])

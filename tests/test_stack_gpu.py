@@ -16,7 +16,7 @@ from moe_decode_weight_gb300 import api, synth
 from oracle import lm_head as OL
 from oracle import stack as OS
 
-from _cases import Layer, bf16_to_np
+from _cases import Layer, assert_bar, bf16_to_np, norm_rounding_allowance
 
 pytestmark = pytest.mark.gpu
 H = 2560
@@ -74,12 +74,13 @@ def test_stack_teacher_forced(model, m):
     xf = OS.rmsnorm_bf16(rs[L])
     lo = OL.lm_head_fp8_logits(qo, so, xf)
     lgn = lg.cpu().numpy()
-    assert np.max(np.abs(lgn - lo)) < 1e-2
+    allow = norm_rounding_allowance(rs[L], qo, so)
+    assert_bar(lgn, lo, "stack head logits", extra=allow)
     order = np.stack([np.lexsort((np.arange(V), -lo[t])) for t in range(m)])
     tin = ti.cpu().numpy()
     for t in range(m):
         vals = lo[t, order[t, :k + 1]]
-        clean = -np.diff(vals) > 1e-3
+        clean = -np.diff(vals) > 1e-3 + 2 * allow[t].max()
         # compare the prefix of the ranking whose margins are all clean
         n = k if clean.all() else int(np.argmin(clean))
         assert np.array_equal(tin[t, :n], order[t, :n]), f"token {t}"
@@ -147,11 +148,12 @@ def test_stack_m32_imposed_routing_with_head(model):
         r_next, _, res = OS.layer_step(rs[l][toks], layer.oracle_dict(), layer.K, topk_override=ov[l][toks])
         _check_residual(rs[l + 1][toks], r_next, res["y"], f"layer {l}")
     lo = OL.lm_head_fp8_logits(qo, so, OS.rmsnorm_bf16(rs[L]))
-    assert np.max(np.abs(lg.cpu().numpy() - lo)) < 1e-2
+    allow = norm_rounding_allowance(rs[L], qo, so)
+    assert_bar(lg.cpu().numpy(), lo, "stack head logits (32 tokens)", extra=allow)
     tin, amn = ti.cpu().numpy(), am.cpu().numpy()
     for t in range(m):
         order = np.lexsort((np.arange(V), -lo[t]))
-        clean = -np.diff(lo[t, order[:k + 1]]) > 1e-3
+        clean = -np.diff(lo[t, order[:k + 1]]) > 1e-3 + 2 * allow[t].max()
         n = k if clean.all() else int(np.argmin(clean))
         assert np.array_equal(tin[t, :n], order[:n]), f"token {t}"
         if clean[0]:

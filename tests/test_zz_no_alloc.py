@@ -34,7 +34,10 @@ def _reference(layer, x):
 
 
 def test_noalloc_matches_workspace_entry_point_twice(layer):
-    xs = [hidden_with_gap(70, 1, layer.wr, layer.K).cuda(), hidden_with_gap(71, 4, layer.wr, layer.K).cuda()]
+    # the largest window first (it fills the most of the shared array), then smaller ones: the
+    # leftovers of an earlier, larger call must not leak into a later one
+    xs = [hidden_with_gap(73, 32, layer.wr, layer.K).cuda(), hidden_with_gap(74, 16, layer.wr, layer.K).cuda(),
+          hidden_with_gap(70, 1, layer.wr, layer.K).cuda(), hidden_with_gap(71, 4, layer.wr, layer.K).cuda()]
     refs = [_reference(layer, x) for x in xs]
     for x, (y_ref, ids_ref) in zip(xs, refs):             # two calls in a row
         m = x.shape[0]
