@@ -230,7 +230,9 @@ def time_e2e(st: Stepper, steps: int, warmup: int):
 
 def oracle_sample(m: int = 1, n_layers: int = 8, frac: int = 8):
     """Time the float64 oracle on a bounded sample of the M-token step: n_layers of the 42
-    layers and a fraction of the head's rows; extrapolated to one full step."""
+    layers and 1/frac of the head's rows. Returns the measured seconds of the sample and the
+    µs per token of the whole step extrapolated from it (layers x 42/n_layers, head x frac);
+    n_layers = 42 and frac = 1 time the whole step."""
     from moe_decode_weight_gb300 import synth
     from oracle import lm_head as OL
     from oracle import stack as OS
@@ -252,22 +254,32 @@ def oracle_sample(m: int = 1, n_layers: int = 8, frac: int = 8):
     for layer in layers:
         rr, _, _ = OS.layer_step(rr, layer, K_ROUTE)
     rows = V // frac
-    w = synth.lm_head_weight(1, rows).float().numpy()    # the first rows of the same stream
+    # the head's codes: the oracle quantises the first 1/8 of the rows once (untimed: the head
+    # is quantised at init) and, for a larger sample, repeats them (the GEMV's cost does not
+    # depend on the values)
+    base = synth.lm_head_weight(1, min(rows, V // 8)).float().numpy()
+    qb, sb = OL.quantize_lm_head(base)
+    reps = -(-rows // qb.shape[0])
+    q, s = np.tile(qb, (reps, 1))[:rows], np.tile(sb, reps)[:rows]
     t0 = time.perf_counter()
     rr = r
+    layer_s = []
     for layer in layers:
+        ta = time.perf_counter()
         rr, _, _ = OS.layer_step(rr, layer, K_ROUTE)
+        layer_s.append(time.perf_counter() - ta)
     t1 = time.perf_counter()
-    q, s = OL.quantize_lm_head(w)           # untimed: the head is quantised once at init
-    t2 = time.perf_counter()
     OL.lm_head_fp8_logits(q, s, OS.rmsnorm_bf16(rr))
-    t3 = time.perf_counter()
-    per_step_s = (t1 - t0) * (L_DEFAULT / n_layers) + (t3 - t2) * frac
+    t2 = time.perf_counter()
+    per_step_s = (t1 - t0) * (L_DEFAULT / n_layers) + (t2 - t1) * frac
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return dict(us_per_token=per_step_s * 1e6 / m, cores=cores,
-                sample=f"{n_layers} of {L_DEFAULT} layers (M={m}) + 1/{frac} of the 157,184 head rows, "
-                       f"float64 numpy oracle, extrapolated to one full step",
-                cpu_seconds=(t1 - t0) + (t3 - t2))
+    whole = n_layers == L_DEFAULT and frac == 1
+    sample = (f"the whole M={m} step: {L_DEFAULT} layers and the 157,184-row head GEMV, float64 numpy oracle"
+              if whole else
+              f"{n_layers} of {L_DEFAULT} layers (M={m}) + 1/{frac} of the 157,184 head rows, float64 numpy "
+              f"oracle; value extrapolated to one full step (layers x {L_DEFAULT / n_layers:g}, head x {frac})")
+    return dict(us_per_token=per_step_s * 1e6 / m, cores=cores, sample=sample, whole=whole,
+                cpu_seconds=t2 - t0, layer_us=float(np.mean(layer_s)) * 1e6, head_us=(t2 - t1) * 1e6 * frac)
 
 
 # ----------------------------------------------------------------------------- arms
@@ -276,15 +288,20 @@ def oracle_sample(m: int = 1, n_layers: int = 8, frac: int = 8):
 def run_reference(args, rank: int):
     if rank != 0:
         return
+    # each step is a bounded sample of the decode step (2 of the 42 layers, 1/32 of the head
+    # rows), so that --steps K --warmup W ends within minutes; ms_per_step is the measured wall
+    # time of that sample and value the µs per token of the whole step extrapolated from it
     res = []
     for i in range(args.warmup + args.steps):
         r = oracle_sample(m=args.m, n_layers=2, frac=32)
         if i >= args.warmup:
             res.append(r)
     us = float(np.median([r["us_per_token"] for r in res]))
+    ms_sample = float(np.median([r["cpu_seconds"] for r in res])) * 1000.0
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/token",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": us * args.m / 1000.0, "higher_is_better": False, "scaling": "weak",
+            "ms_per_step": ms_sample, "ms_per_step_is": "measured wall time of one sampled step",
+            "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": _workload(args.m), "M": args.m},
             "cpu_baseline": {"value": us, "unit": "us/token", "cores": res[0]["cores"], "kind": "oracle",
@@ -318,6 +335,78 @@ def sweep(layers, head, device, ms=(1, 2, 4, 8, 16, 32), steps: int = 3, warmup:
                          "layer_stack_gbs": float(np.mean(r["bytes_layers"])) / (lay * 1e6)})
             del st
         out[routing] = rows
+    return out
+
+
+def union_routing(layer: int, m: int, union: int) -> np.ndarray:
+    """Imposed routing of a verify window whose union has `union` routed experts: the M tokens
+    fall into groups that share one set of K experts (groups [0,0,0,0], [0,0,1,1],
+    [0,0,1,2], [0,1,2,3] for 8/16/24/32 at M = 4); the sets are disjoint draws of a seeded
+    permutation (seed 2 + layer). int32 [M, K]."""
+    groups = {8: [0, 0, 0, 0], 16: [0, 0, 1, 1], 24: [0, 0, 1, 2], 32: [0, 1, 2, 3]}[union][:m]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([2, layer, 606])))
+    perm = rng.permutation(E)
+    return np.stack([np.sort(perm[K_ROUTE * g:K_ROUTE * (g + 1)]) for g in groups]).astype(np.int32)
+
+
+def time_single_layer(layers, device, m: int, union=None, reps: int = 4):
+    """One MoE layer per moe_decode_layer call (one launch each), cycling through the resident
+    layers so no call finds its weights in L2 (42 x >= 30.8 MB >> 129 MB). union=None: the
+    router decides (config 0); else the window's union is imposed per layer (config 2).
+    Returns mean µs per call (launch included), the realised union and the achieved GB/s."""
+    from moe_decode_weight_gb300 import api, roofline as R, synth
+    L = len(layers)
+    x = synth.hidden_states(0 if union is None else 2, m, 0).to(device)
+    y = torch.empty((m, 2560), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(api.mdw_moe_workspace_bytes(layers[0], m), dtype=torch.uint8, device=device)
+    ovs = [None if union is None else torch.from_numpy(union_routing(l, m, union)).to(device) for l in range(L)]
+    unions = []
+    for l in range(L):                                  # warm-up; realised unions
+        api.moe_decode_layer(layers[l], x, y, ws, topk_override=ovs[l])
+        torch.cuda.synchronize()
+        hdr = ws[:1024].cpu().numpy().view(np.uint32)
+        if int(hdr[0]) != 0:
+            raise RuntimeError(f"device status {api.STATUS.get(int(hdr[0]))}")
+        unions.append(int(hdr[4]))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        for l in range(L):
+            api.moe_decode_layer(layers[l], x, y, ws, topk_override=ovs[l])
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / (reps * L)
+    b = float(np.mean([R.moe_layer_bytes(u, m) for u in unions]))
+    return {"M": m, "us_per_layer": us, "union": float(np.mean(unions)), "bytes": b,
+            "achieved_gbs": b / (us * 1e3), "calls": reps * L}
+
+
+def time_heads(head, w_bf16, device, m: int = 1, reps: int = 20):
+    """The FP8 head and the BF16 head (the pages' 2x byte comparison) on the same hidden
+    state: µs per call and achieved GB/s of each (weights + row scales + input + logits)."""
+    from moe_decode_weight_gb300 import api, roofline as R, synth
+    bf = api.mdw_lm_head_bf16_init(w_bf16)
+    x = _rmsnorm_bf16(synth.hidden_states(1, m, 0).to(device))
+    out = {}
+    for name, fn, hd, nbytes in (("fp8", api.lm_head_fp8, head, R.head_fp8_bytes(m)),
+                                 ("bf16", api.lm_head_bf16, bf, R.head_bf16_bytes(m))):
+        ws = torch.zeros(api.mdw_lm_head_workspace_bytes(hd, m, TOPK_VOCAB), dtype=torch.uint8, device=device)
+        am = torch.zeros(m, dtype=torch.int32, device=device)
+        ti = torch.zeros((m, TOPK_VOCAB), dtype=torch.int32, device=device)
+        lg = torch.zeros((m, V), dtype=torch.float32, device=device)
+        for _ in range(3):
+            fn(hd, x, am, ws, logits=lg, topk=TOPK_VOCAB, topk_idx=ti)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn(hd, x, am, ws, logits=lg, topk=TOPK_VOCAB, topk_idx=ti)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / reps
+        out[name] = {"us": us, "bytes": nbytes, "achieved_gbs": nbytes / (us * 1e3)}
+    out["bytes_ratio_bf16_over_fp8"] = out["bf16"]["bytes"] / out["fp8"]["bytes"]
+    out["time_ratio_bf16_over_fp8"] = out["bf16"]["us"] / out["fp8"]["us"]
+    out["M"] = m
     return out
 
 
@@ -463,6 +552,14 @@ def run_gpu(args, rank: int, world: int):
         del st4
 
     if not args.no_extras and args.m == 1:
+        extra["single_layer"] = {
+            "config0_m1": time_single_layer(layers, device, 1),
+            "config2_m4_unions": [time_single_layer(layers, device, 4, union=u) for u in (8, 16, 24, 32)],
+            "how": "one moe_decode_layer launch per call, cycling through the 42 resident layers "
+                   "(no call finds its weights in L2); config 2's unions imposed per layer",
+        }
+        extra["heads_m1"] = time_heads(head, _w_bf16, device, m=1)
+        extra["heads_m4"] = time_heads(head, _w_bf16, device, m=4)
         extra["sampler"] = time_sampler(head, st, device)
         extra["fp8_vs_bf16"] = fp8_vs_bf16(head, _w_bf16, device)
         extra["sweep"] = sweep(layers, head, device)
@@ -472,9 +569,10 @@ def run_gpu(args, rank: int, world: int):
     cpu = None
     if world == 1 and not args.no_cpu:
         try:
-            o = oracle_sample(m=args.m)
+            o = oracle_sample(m=args.m, n_layers=L_DEFAULT if args.layers == L_DEFAULT else args.layers, frac=1)
             cpu = {"value": o["us_per_token"], "unit": "us/token", "cores": o["cores"], "kind": "oracle",
-                   "sample": o["sample"]}
+                   "sample": o["sample"], "cpu_seconds": o["cpu_seconds"],
+                   "per_config_us": {"config0_one_layer_m1": o["layer_us"], "config1_head_m1": o["head_us"]}}
         except Exception as e:        # the baseline is reported, not required
             cpu = {"value": None, "unit": "us/token", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
     line = {

@@ -33,6 +33,13 @@ MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
   l.header = take(kHdrWords * 4);
+  w.xr = w.xz = w.xh = 0;
+  if (M <= kStreamMaxM) {                   // zeroed with the header before every launch
+    w.xr = take((size_t)M * (kH / 2) * 8);
+    w.xz = take((size_t)M * E * 8);
+    w.xh = take(P * kI * 8);
+  }
+  w.zero_end = o;
   l.xq = take((size_t)M * kH);
   l.sx = take((size_t)M * 4);
   l.logits = take((size_t)M * E * 4);
@@ -101,7 +108,11 @@ void fill_layer(LayerDesc& d, const mdw_moe_weights* w) {
   d.sh_w2_s = static_cast<const uint8_t*>(w->sh_w2_s);
 }
 
-void fill_ws(MoeParams& p, const mdw_moe_ws_layout& l, uint8_t* base) {
+}  // namespace
+
+namespace mdw {
+void fill_moe_ws(MoeParams& p, const MoeWs& w, uint8_t* base) {
+  const mdw_moe_ws_layout& l = w.lay;
   p.hdr = reinterpret_cast<uint32_t*>(base + l.header);
   p.xq = base + l.xq;
   p.sx = reinterpret_cast<float*>(base + l.sx);
@@ -115,7 +126,13 @@ void fill_ws(MoeParams& p, const mdw_moe_ws_layout& l, uint8_t* base) {
   p.h = reinterpret_cast<float*>(base + l.h);
   p.hq = base + l.hq;
   p.sh = reinterpret_cast<float*>(base + l.sh);
+  p.xr = w.xr ? reinterpret_cast<uint64_t*>(base + w.xr) : nullptr;
+  p.xz = w.xz ? reinterpret_cast<uint64_t*>(base + w.xz) : nullptr;
+  p.xh = w.xh ? reinterpret_cast<uint64_t*>(base + w.xh) : nullptr;
 }
+}  // namespace mdw
+
+namespace {
 
 struct Draw {                     // optional draw on the final top-k
   const double* u = nullptr;
@@ -246,9 +263,9 @@ mdw_status moe_decode_layer(const mdw_moe_weights* w, int32_t M, const void* x_b
   p->ids_out = topk_ids_out;
   p->gates_out = topk_w_out;
   uint8_t* base = static_cast<uint8_t*>(ws);
-  fill_ws(*p, lay.lay, base);
+  fill_moe_ws(*p, lay, base);
   st = MDW_OK;
-  if (cudaMemsetAsync(base + lay.lay.header, 0, kHdrWords * 4, s) != cudaSuccess) st = MDW_ERR_CUDA;
+  if (cudaMemsetAsync(base + lay.lay.header, 0, lay.zero_end - lay.lay.header, s) != cudaSuccess) st = MDW_ERR_CUDA;
   if (st == MDW_OK) st = cuda_status(launch_moe(*p, s));
   delete p;
   return st;
@@ -404,9 +421,9 @@ mdw_status moe_decode_stack_routed(const mdw_moe_weights* layers, int32_t L, con
     p->resid = reinterpret_cast<__nv_bfloat16*>(base + lay.resid);
     p->resid_pingpong = 1;
   }
-  fill_ws(*p, lay.lay, base);
+  fill_moe_ws(*p, lay, base);
   st = MDW_OK;
-  if (cudaMemsetAsync(base + lay.lay.header, 0, kHdrWords * 4, s) != cudaSuccess) st = MDW_ERR_CUDA;
+  if (cudaMemsetAsync(base + lay.lay.header, 0, lay.zero_end - lay.lay.header, s) != cudaSuccess) st = MDW_ERR_CUDA;
   if (st == MDW_OK && resid_out &&
       cudaMemcpyAsync(resid_out, r0_bf16, (size_t)M * kH * 2, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     st = MDW_ERR_CUDA;

@@ -51,9 +51,11 @@ extern "C" mdw_status moe_decode_layer_noalloc(const mdw_moe_weights* w, int32_t
                                                float* topk_w_out, uint32_t* device_status_out,
                                                mdw_stream_t stream) {
   // shape and weight checks (format tag, M range, ...) and the scratch layout of this call
-  mdw_moe_ws_layout lay;
-  mdw_status st = mdw_moe_workspace_layout(w, M, &lay);
+  mdw_moe_ws_layout pub;
+  mdw_status st = mdw_moe_workspace_layout(w, M, &pub);
   if (st != MDW_OK) return st;
+  const MoeWs ws = moe_ws_layout(M, w->num_experts, w->top_k, false, 1);
+  const mdw_moe_ws_layout& lay = ws.lay;
   if (lay.total > MDW_NOALLOC_SCRATCH_BYTES) return MDW_ERR_WORKSPACE_TOO_SMALL;
   if (!x_bf16 || !y || !aligned16_or_null(x_bf16) || !aligned16_or_null(y) || !aligned16_or_null(residual) ||
       !aligned16_or_null(topk_override) || !aligned16_or_null(topk_ids_out) ||
@@ -87,21 +89,10 @@ extern "C" mdw_status moe_decode_layer_noalloc(const mdw_moe_weights* w, int32_t
   p.topk_override = topk_override;
   p.ids_out = topk_ids_out;
   p.gates_out = topk_w_out;
-  p.hdr = reinterpret_cast<uint32_t*>(base + lay.header);
-  p.xq = base + lay.xq;
-  p.sx = reinterpret_cast<float*>(base + lay.sx);
-  p.logits = reinterpret_cast<float*>(base + lay.logits);
-  p.ids = reinterpret_cast<int32_t*>(base + lay.ids);
-  p.gates = reinterpret_cast<float*>(base + lay.gates);
-  p.slot_expert = reinterpret_cast<int32_t*>(base + lay.slot_expert);
-  p.pair_token = reinterpret_cast<int32_t*>(base + lay.pair_token);
-  p.pair_slot = reinterpret_cast<int32_t*>(base + lay.pair_slot);
-  p.pair_gate = reinterpret_cast<float*>(base + lay.pair_gate);
-  p.h = reinterpret_cast<float*>(base + lay.h);
-  p.hq = base + lay.hq;
-  p.sh = reinterpret_cast<float*>(base + lay.sh);
-  // the status word and the grid-barrier counter must start at zero on every call
-  if (cudaMemsetAsync(base + lay.header, 0, kHdrWords * 4, s) != cudaSuccess) return MDW_ERR_CUDA;
+  fill_moe_ws(p, ws, base);
+  // the status word, the grid-barrier counter and the tagged exchange words must start at
+  // zero on every call
+  if (cudaMemsetAsync(base + lay.header, 0, ws.zero_end - lay.header, s) != cudaSuccess) return MDW_ERR_CUDA;
   if (launch_moe(p, s) != cudaSuccess) return MDW_ERR_CUDA;
   if (device_status_out &&
       cudaMemcpyAsync(device_status_out, base + lay.header, 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
