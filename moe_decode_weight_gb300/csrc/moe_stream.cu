@@ -72,6 +72,32 @@ static_assert(2 * kTileW + 2 * kTileS <= kSlotBytes, "a tile must fit a ring slo
 
 __host__ __device__ constexpr int ring_slots(int maxm) { return maxm <= 2 ? 6 : 5; }
 
+// ------------------------------------------------------------------ phase trace
+
+// Built only with -DMDW_TRACE (the profiling library, never the product build): thread 0 of
+// every block records %globaltimer at each phase boundary of every layer.
+#ifdef MDW_TRACE
+// clock64 at each phase boundary of each layer (thread 0), kept in shared memory during the
+// launch and written out at its end, so the stamps add no global traffic
+constexpr int kSTraceLayers = 64, kSTracePoints = 20, kSTraceBlocks = 256;
+__device__ unsigned long long g_strace[kSTraceLayers * kSTracePoints * kSTraceBlocks];
+__shared__ unsigned long long s_strace[kSTraceLayers * kSTracePoints];
+#define STRACE(layer, point)                                                                   \
+  do {                                                                                         \
+    if (threadIdx.x == 0 && (layer) < kSTraceLayers) s_strace[(layer) * kSTracePoints + (point)] = clock64(); \
+  } while (0)
+#define STRACE_FLUSH(nl)                                                                       \
+  do {                                                                                         \
+    __syncthreads();                                                                           \
+    if (blockIdx.x < kSTraceBlocks)                                                            \
+      for (int i_ = threadIdx.x; i_ < (nl) * kSTracePoints && i_ < kSTraceLayers * kSTracePoints; i_ += blockDim.x) \
+        g_strace[(i_ / kSTracePoints * kSTracePoints + i_ % kSTracePoints) * kSTraceBlocks + blockIdx.x] = s_strace[i_]; \
+  } while (0)
+#else
+#define STRACE(layer, point) do { } while (0)
+#define STRACE_FLUSH(nl) do { } while (0)
+#endif
+
 // ------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -88,6 +114,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
                : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
+// Orders this thread's (and, after a barrier, the block's) earlier generic accesses to shared
+// memory before later asynchronous-proxy (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // [dst, dst + bytes) <- [src, src + bytes): one bulk asynchronous copy (16-byte aligned, a
 // multiple of 16 bytes), its bytes counted on `bar`
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -97,13 +126,15 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void st_word(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
+// Poll loads. A poll issues all of its loads before it looks at any of them: a load whose
+// predicate depended on the previous word's check would wait a full L2 round trip per word.
 __device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
   uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ void ld_word2(const uint64_t* p, uint64_t& a, uint64_t& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
 }
 __device__ __forceinline__ uint64_t tagged(uint32_t payload, uint32_t tag) {
   return ((uint64_t)tag << 32) | payload;
@@ -129,9 +160,10 @@ struct SLayout {
   static constexpr size_t dleft = dres + (size_t)kMaxPairs * kDnParts * 16 * 4;
   static constexpr size_t rres = dleft + (size_t)kMaxPairs * (kMaxRows - 16) * 4;   // [M][kMaxRows] fp32
   static constexpr size_t cand = rres + (size_t)MAXM * kMaxRows * 4;               // top-k scratch
-  static constexpr size_t tabs = cand + (size_t)MAXM * 128 * 8;
+  static constexpr size_t zrow = cand + (size_t)MAXM * 128 * 8;                    // polled logits [M][E] fp32
+  static constexpr size_t tabs = zrow + (size_t)MAXM * MDW_MAX_EXPERTS * 4;
   static constexpr size_t bars = tabs + 4096;                                      // mbarriers, counters
-  static constexpr size_t total = bars + (size_t)NS * 16 + 16;
+  static constexpr size_t total = bars + (size_t)NS * 16 + 16 + 16;   // + the router barrier
 };
 
 struct STables {
@@ -155,6 +187,7 @@ static_assert(sizeof(STables) <= 4096, "tables exceed their shared-memory region
 // Per-block pipeline state (the pointers and `seq` are identical in all threads).
 struct Ring {
   uint64_t* full;        // [NS] mbarriers: one phase per item requested into the slot
+  uint64_t* rbar;        // mbarrier of the router rows' copy (one phase per layer)
   int* done;             // [NS] finished units of the item in the slot
   uint32_t* item;        // [NS] ring sequence number of the item last requested into the slot
   uint32_t seq;          // items of all layers so far
@@ -228,6 +261,7 @@ __device__ void issue_item(const MoeParams& p, const LayerDesc& L, const STables
   uint8_t* dst = smem + SL::ring + (size_t)s * kSlotBytes;
   uint64_t* bar = rg.full + s;
   *reinterpret_cast<volatile uint32_t*>(rg.item + s) = g;
+  fence_proxy_async();
   if (it < pl.n_gu) {
     const int t = pl.t0 + it, slot = t / kTilesPerSlot, j0 = (t % kTilesPerSlot) * kTileRP;
     const int e = tb.slot_expert[slot];
@@ -254,11 +288,13 @@ __device__ void issue_item(const MoeParams& p, const LayerDesc& L, const STables
 }
 
 // After a failure: wait (bounded by the default budget, not the caller's) until the last
-// item requested into every slot has landed (the slot's earlier items have), so no copy
-// writes shared memory after the block exits. Called by every thread after a block barrier.
+// item requested into every slot has landed (the slot's earlier items have), and the layer's
+// router-row copy, so no copy writes shared memory after the block exits. Every thread of the
+// block calls it after the same block barrier.
 template <int MAXM>
-__device__ void drain_ring(const Ring& rg) {
+__device__ void drain_ring(const Ring& rg, int layer, bool router_copy) {
   using SL = SLayout<MAXM>;
+  __syncthreads();
   if (threadIdx.x != 0) return;
   for (int s = 0; s < SL::NS; ++s) {
     const uint32_t g = ld_volatile_shared(rg.item + s);
@@ -267,6 +303,10 @@ __device__ void drain_ring(const Ring& rg) {
     while (!mbar_test(rg.full + s, (g / SL::NS) & 1))
       if (clock64() - t0 > kSpinBudget) break;
   }
+  if (!router_copy) return;
+  const long long t0 = clock64();
+  while (!mbar_test(rg.rbar, layer & 1))
+    if (clock64() - t0 > kSpinBudget) break;
 }
 
 // ------------------------------------------------------------------ P0: input
@@ -285,25 +325,42 @@ __device__ bool prepare_input(const MoeParams& p, int layer, uint8_t* smem, STab
   const uint4* src = reinterpret_cast<const uint4*>(p.stack_mode ? p.r0 : p.x_in);
   // 1. rows into shared memory (a chunk = 8 bf16 = 4 tagged words when polled)
   if (poll) {
+    // every chunk of this thread is requested before any is checked; missing chunks are
+    // requested again together
+    constexpr int NCH = (MAXM * CPT + kThreads - 1) / kThreads;
     const uint64_t* xr = p.xr;
     const uint32_t tag = (uint32_t)layer;
+    uint32_t want = 0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k)
+      if ((int)threadIdx.x + k * kThreads < M * CPT) want |= 1u << k;
+    long long t0 = 0;
     bool ok = true;
-    for (int c = threadIdx.x; c < M * CPT && ok; c += blockDim.x) {
-      uint64_t w[4];
-      ld_word2(xr + 4 * (size_t)c, w[0], w[1]);
-      ld_word2(xr + 4 * (size_t)c + 2, w[2], w[3]);
-      if (tag_of(w[0]) != tag || tag_of(w[1]) != tag || tag_of(w[2]) != tag || tag_of(w[3]) != tag) {
-        const long long t0 = clock64();
-        int n = 0;
-        for (;;) {
-          ld_word2(xr + 4 * (size_t)c, w[0], w[1]);
-          ld_word2(xr + 4 * (size_t)c + 2, w[2], w[3]);
-          if (tag_of(w[0]) == tag && tag_of(w[1]) == tag && tag_of(w[2]) == tag && tag_of(w[3]) == tag) break;
-          if ((++n & 15) == 0 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) { ok = false; break; }
-          if (clock64() - t0 > p.spin_budget) { set_status(p.hdr, MDW_ERR_TIMEOUT); ok = false; break; }
+    for (int n = 0; want != 0; ++n) {
+      uint64_t w[NCH][4];
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) {
+        const size_t c = threadIdx.x + (size_t)k * kThreads;
+        if (want & (1u << k)) {
+          ld_word2(xr + 4 * c, w[k][0], w[k][1]);
+          ld_word2(xr + 4 * c + 2, w[k][2], w[k][3]);
         }
       }
-      xb4[c] = make_uint4((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
+      uint32_t got = 0;
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) {
+        const int c = threadIdx.x + k * kThreads;
+        if ((want & (1u << k)) && tag_of(w[k][0]) == tag && tag_of(w[k][1]) == tag && tag_of(w[k][2]) == tag &&
+            tag_of(w[k][3]) == tag) {
+          xb4[c] = make_uint4((uint32_t)w[k][0], (uint32_t)w[k][1], (uint32_t)w[k][2], (uint32_t)w[k][3]);
+          got |= 1u << k;
+        }
+      }
+      want &= ~got;
+      if (want == 0) break;
+      if (n == 0) t0 = clock64();
+      if ((n & 15) == 15 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) { ok = false; break; }
+      if (clock64() - t0 > p.spin_budget) { set_status(p.hdr, MDW_ERR_TIMEOUT); ok = false; break; }
     }
     if (!ok) atomicExch(&tb.fail, 1);
   } else {
@@ -400,15 +457,10 @@ __device__ __forceinline__ void router_range(int E, int& e0, int& e1) {
   e0 = (int)((long long)blockIdx.x * E / gridDim.x);
   e1 = (int)((long long)(blockIdx.x + 1) * E / gridDim.x);
 }
-__device__ __forceinline__ void load_router_row(const LayerDesc& L, int e, uint4 (&wv)[10]) {
-  const uint4* wr = reinterpret_cast<const uint4*>(L.router_w + (size_t)e * kH);
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 10; ++i) wv[i] = ldg_stream16(wr + 32 * i + lane);
-}
-// Warp w: router rows e0 + w, e0 + w + 12, ...; the first row's weights are in `wv` already.
+// The block's router rows [e0, e1) (at most 4 x 5 KB) are bulk-copied into ring slot 0 at the
+// start of the layer (the ring is idle until the routing is known) and read from there.
 template <int MAXM>
-__device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, uint4 (&wv)[10], int layer) {
+__device__ bool router_rows(const MoeParams& p, const uint8_t* smem, const Ring& rg, int layer) {
   using SL = SLayout<MAXM>;
   const int M = p.M, E = p.E;
   int e0, e1;
@@ -416,15 +468,17 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem + SL::xb);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tag = (uint32_t)layer + 1;
+  if (e0 + warp < e1 && !wait_full(rg.rbar, layer & 1, p)) return false;
   for (int e = e0 + warp; e < e1; e += kWarps) {
-    if (e != e0 + warp) load_router_row(L, e, wv);
+    const uint4* w4 = reinterpret_cast<const uint4*>(smem + SL::ring + (size_t)(e - e0) * kH * 2);
     for (int t = 0; t < M; ++t) {
       const uint4* x4 = reinterpret_cast<const uint4*>(xb + (size_t)t * kH);
       float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 10; ++i) {
+        const uint4 wv = w4[32 * i + lane];
         const uint4 xv = x4[32 * i + lane];
-        const uint32_t a[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+        const uint32_t a[4] = {wv.x, wv.y, wv.z, wv.w};
         const uint32_t b[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -439,45 +493,46 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
       }
     }
   }
+  return true;
 }
 
 // ------------------------------------------------------------------ P2: routing
 
-// Polls token t's E logits (tag layer + 1) into v[] (lane + 32 j); false on timeout/failure.
-__device__ bool poll_logits(const MoeParams& p, int t, int layer, float (&v)[MDW_MAX_EXPERTS / 32]) {
-  constexpr int PER = MDW_MAX_EXPERTS / 32;
-  const int lane = threadIdx.x & 31, E = p.E;
+// Every thread of the block polls its share of the M x E logit words (tag layer + 1), all
+// of them requested before any is checked, into zrow (fp32); false (tb.fail set) on timeout or
+// when another block failed. Every thread of the block must call it.
+template <int MAXM>
+__device__ bool poll_logits(const MoeParams& p, int layer, float* zrow, STables& tb) {
+  constexpr int NW = (MAXM * MDW_MAX_EXPERTS + kThreads - 1) / kThreads;
+  const int n_words = p.M * p.E;
   const uint32_t tag = (uint32_t)layer + 1;
-  const uint64_t* z = p.xz + (size_t)t * E;
-  uint32_t missing = 0;
+  uint32_t want = 0;
 #pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = -INFINITY;
-    if (e < E) {
-      const uint64_t w = ld_word(z + e);
-      if (tag_of(w) == tag) v[j] = __uint_as_float((uint32_t)w);
-      else missing |= 1u << j;
-    }
-  }
+  for (int k = 0; k < NW; ++k)
+    if ((int)threadIdx.x + k * kThreads < n_words) want |= 1u << k;
   long long t0 = 0;
-  int n = 0;
-  while (__any_sync(0xffffffffu, missing != 0)) {
-    if (n == 0) t0 = clock64();
+  for (int n = 0; want != 0; ++n) {
+    uint64_t w[NW];
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      if (missing & (1u << j)) {
-        const uint64_t w = ld_word(z + lane + 32 * j);
-        if (tag_of(w) == tag) { v[j] = __uint_as_float((uint32_t)w); missing &= ~(1u << j); }
+    for (int k = 0; k < NW; ++k) w[k] = (want & (1u << k)) ? ld_word(p.xz + threadIdx.x + k * kThreads) : 0;
+    uint32_t got = 0;
+#pragma unroll
+    for (int k = 0; k < NW; ++k)
+      if ((want & (1u << k)) && tag_of(w[k]) == tag) {
+        zrow[threadIdx.x + k * kThreads] = __uint_as_float((uint32_t)w[k]);
+        got |= 1u << k;
       }
+    want &= ~got;
+    if (want == 0) break;
+    if (n == 0) t0 = clock64();
+    if (((n & 15) == 15 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) || *reinterpret_cast<volatile int*>(&tb.fail)) {
+      atomicExch(&tb.fail, 1);
+      break;
     }
-    ++n;
-    bool bad = false;
-    if ((n & 15) == 0 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) bad = true;
-    if (clock64() - t0 > p.spin_budget) { if (lane == 0) set_status(p.hdr, MDW_ERR_TIMEOUT); bad = true; }
-    if (__any_sync(0xffffffffu, bad)) return false;
+    if (clock64() - t0 > p.spin_budget) { set_status(p.hdr, MDW_ERR_TIMEOUT); atomicExch(&tb.fail, 1); break; }
   }
-  return true;
+  __syncthreads();
+  return tb.fail == 0;
 }
 
 // Top-K of one token's logits held by the warp (v[j] = logit lane + 32 j), ties -> lower id:
@@ -485,7 +540,8 @@ __device__ bool poll_logits(const MoeParams& p, int t, int layer, float (&v)[MDW
 // logits reach T, so the K-th largest logit does too); the logits not worse than T (usually
 // little more than K) are compacted into shared memory and ranked among themselves. Writes
 // the ids and raw logits of ranks 0..K-1 to tb.ids / tb.gts [t * K + r].
-__device__ void topk_token(float (&v)[MDW_MAX_EXPERTS / 32], int E, int K, int t, STables& tb, float* cv, int* ci) {
+__device__ __forceinline__ void topk_token(float (&v)[MDW_MAX_EXPERTS / 32], int E, int K, int t, STables& tb, float* cv, int* ci,
+                           int layer = 0) {
   constexpr int PER = MDW_MAX_EXPERTS / 32;
   constexpr int kCand = 128;
   const int lane = threadIdx.x & 31;
@@ -557,14 +613,14 @@ __device__ bool route_window(const MoeParams& p, STables& tb, int layer, uint8_t
   using SL = SLayout<MAXM>;
   const int M = p.M, E = p.E, K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) { tb.bad = 0; tb.fail = 0; }
+  if (threadIdx.x == 0) tb.bad = 0;
   __syncthreads();
+  float* zrow = reinterpret_cast<float*>(smem + SL::zrow);
+  if (!poll_logits<MAXM>(p, layer, zrow, tb)) return false;
+  STRACE(layer, 3);
   if (warp < M) {
     const int t = warp;
-    float v[MDW_MAX_EXPERTS / 32];
-    if (!poll_logits(p, t, layer, v)) {
-      if (lane == 0) atomicExch(&tb.fail, 1);
-    } else if (p.topk_override) {
+    if (p.topk_override) {
       const int32_t* ov = p.topk_override + (p.stack_mode ? (size_t)layer * M * K : 0);
       if (lane < K) {
         int id = ov[t * K + lane];
@@ -573,23 +629,17 @@ __device__ bool route_window(const MoeParams& p, STables& tb, int layer, uint8_t
           if (j != lane && ov[t * K + j] == id) ok = false;
         if (!ok) { atomicExch(&tb.bad, 1); id = 0; }
         tb.ids[t * K + lane] = id;
-      }
-      __syncwarp();
-      // the logit of each imposed id, from the register-held row (lane id & 31, entry id >> 5)
-      for (int r = 0; r < K; ++r) {
-        const int id = tb.ids[t * K + r];
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < MDW_MAX_EXPERTS / 32; ++j)
-          if (j == (id >> 5)) z = v[j];
-        z = __shfl_sync(0xffffffffu, z, id & 31);
-        if (lane == 0) tb.gts[t * K + r] = z;
+        tb.gts[t * K + lane] = zrow[t * E + id];
       }
       __syncwarp();
     } else {
+      float v[MDW_MAX_EXPERTS / 32];
+#pragma unroll
+      for (int j = 0; j < MDW_MAX_EXPERTS / 32; ++j) v[j] = lane + 32 * j < E ? zrow[t * E + lane + 32 * j] : -INFINITY;
       float* cv = reinterpret_cast<float*>(smem + SL::cand) + t * 256;
-      topk_token(v, E, K, t, tb, cv, reinterpret_cast<int*>(cv + 128));
+      topk_token(v, E, K, t, tb, cv, reinterpret_cast<int*>(cv + 128), layer);
     }
+    STRACE(layer, 15);
   }
   __syncthreads();
   if (tb.fail) return false;
@@ -663,8 +713,10 @@ __device__ bool route_window(const MoeParams& p, STables& tb, int layer, uint8_t
       tb.pair_gate[q] = tb.gts[i];
     }
     if (first && lane < M) { tb.pair_token[lane] = lane; tb.pair_gate[lane] = 1.0f; }
+    STRACE(layer, 16);
   }
   __syncthreads();
+  STRACE(layer, 17);
   if (blockIdx.x == 0) {
     // publish the routing (inspection and the optional outputs)
     for (int i = threadIdx.x; i < M * K; i += blockDim.x) {
@@ -775,14 +827,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
   rg.full = reinterpret_cast<uint64_t*>(smem + SL::bars);
   rg.done = reinterpret_cast<int*>(smem + SL::bars + SL::NS * 8);
   rg.item = reinterpret_cast<uint32_t*>(smem + SL::bars + SL::NS * 12);
+  rg.rbar = reinterpret_cast<uint64_t*>(smem + SL::bars + SL::NS * 16 + 16);
   rg.seq = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < SL::NS; ++s) { mbar_init(rg.full + s, 1); rg.done[s] = 0; rg.item[s] = kNoItem; }
+    mbar_init(rg.rbar, 1);
     tb.fail = 0;
     fence_mbar_init();
   }
   __syncthreads();
   Plan pl;
+  bool has_router_rows;
+  {
+    int e0, e1;
+    router_range(p.E, e0, e1);
+    has_router_rows = e1 > e0;
+  }
   pl.r0 = 2 * (int)((long long)blockIdx.x * (kH / 2) / G);
   pl.nrows = 2 * (int)((long long)(blockIdx.x + 1) * (kH / 2) / G) - pl.r0;
   float* part = reinterpret_cast<float*>(smem + SL::part);
@@ -792,16 +852,24 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
 
   for (int layer = 0; layer < p.L; ++layer) {
     const LayerDesc& L = p.layers[layer];
-    uint4 wv[10];
-    {
+    if (threadIdx.x == 0) {
+      // this layer's router rows into ring slot 0 (idle until the routing is known)
       int e0, e1;
       router_range(p.E, e0, e1);
-      if (e0 + warp < e1) load_router_row(L, e0 + warp, wv);
+      if (e1 > e0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(rg.rbar, (uint32_t)(e1 - e0) * kH * 2);
+        bulk_copy(smem + SL::ring, L.router_w + (size_t)e0 * kH, (uint32_t)(e1 - e0) * kH * 2, rg.rbar);
+      }
     }
     pl.base = rg.seq;
-    if (!prepare_input<MAXM>(p, layer, smem, tb, pl)) break;
-    router_rows<MAXM>(p, L, smem, wv, layer);
-    if (!route_window<MAXM>(p, tb, layer, smem)) break;
+    STRACE(layer, 0);
+    if (!prepare_input<MAXM>(p, layer, smem, tb, pl)) { drain_ring<MAXM>(rg, layer, has_router_rows); break; }
+    STRACE(layer, 1);
+    if (!router_rows<MAXM>(p, smem, rg, layer)) atomicExch(&tb.fail, 1);
+    STRACE(layer, 2);
+    if (!route_window<MAXM>(p, tb, layer, smem)) { drain_ring<MAXM>(rg, layer, has_router_rows); break; }
+    STRACE(layer, 4);
     // the block's work: tiles [t0, t0 + n_gu) of S * 96, then its rows of every slot's W2
     const int S = tb.n_slots;
     {
@@ -819,6 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
       if (lane < n0) issue_item<MAXM>(p, L, tb, pl, rg, smem, lane);
     }
     rg.seq = pl.base + pl.n_items;
+    STRACE(layer, 5);
     bool ok = true;
     // P3: gate/up units u = warp, warp + 12, ...: tile u / 10, K part u % 10
     const int n_gu_units = pl.n_gu * kGuParts;
@@ -836,6 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
         if (NT > 1 && 2 + tt < m) xt1 = smem + SL::xh + (size_t)tb.pair_token[pb + 2 + tt] * kXhBytes;
       }
       if (!wait_item<SL::NS>(rg, gs, p)) { ok = false; break; }
+      STRACE(layer, 11);
       const uint8_t* buf = smem + SL::ring + (size_t)s * kSlotBytes;
       float r[4];
       gu_unit<NT>(buf, kp, xt0, xt1, g, q, r);
@@ -867,9 +937,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
         if (lane == 0 && it + SL::NS < pl.n_items) issue_item<MAXM>(p, L, tb, pl, rg, smem, it + SL::NS);
       }
     }
+    STRACE(layer, 12);
     if (!ok) { atomicExch(&tb.fail, 1); }
     __syncthreads();
-    if (tb.fail) { drain_ring<MAXM>(rg); break; }
+    STRACE(layer, 6);
+    if (tb.fail) { drain_ring<MAXM>(rg, layer, has_router_rows); break; }
     // during the h exchange: the next layer's router rows and shared-expert slice into L2
     if (p.stack_mode && layer + 1 < p.L && lane == 0 && warp < 5) {
       const LayerDesc& Ln = p.layers[layer + 1];
@@ -892,36 +964,35 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
       for (int pr = warp; pr < P && ok; pr += kWarps) {
         const uint64_t* hw = p.xh + (size_t)pr * kI;
         float hv[2 * J];
-        uint32_t missing = 0;
+        // two halves of six word pairs per lane, each requested in full before it is checked
+        // (all twelve at once would not fit the register budget)
+        constexpr int JH = J / 2;
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-          uint64_t a, b;
-          ld_word2(hw + 2 * (lane + 32 * j), a, b);
-          hv[2 * j] = __uint_as_float((uint32_t)a);
-          hv[2 * j + 1] = __uint_as_float((uint32_t)b);
-          if (tag_of(a) != tag || tag_of(b) != tag) missing |= 1u << j;
-        }
-        long long t0 = 0;
-        int n = 0;
-        while (__any_sync(0xffffffffu, missing != 0)) {
-          if (n == 0) t0 = clock64();
+        for (int half = 0; half < 2 && ok; ++half) {
+          uint32_t want = (1u << JH) - 1;
+          long long t0 = 0;
+          for (int n = 0;; ++n) {
+            uint64_t w[JH][2];
 #pragma unroll
-          for (int j = 0; j < J; ++j) {
-            if (missing & (1u << j)) {
-              uint64_t a, b;
-              ld_word2(hw + 2 * (lane + 32 * j), a, b);
-              if (tag_of(a) == tag && tag_of(b) == tag) {
-                hv[2 * j] = __uint_as_float((uint32_t)a);
-                hv[2 * j + 1] = __uint_as_float((uint32_t)b);
-                missing &= ~(1u << j);
+            for (int j = 0; j < JH; ++j)
+              if (want & (1u << j)) ld_word2(hw + 2 * (lane + 32 * (half * JH + j)), w[j][0], w[j][1]);
+            uint32_t got = 0;
+#pragma unroll
+            for (int j = 0; j < JH; ++j) {
+              if ((want & (1u << j)) && tag_of(w[j][0]) == tag && tag_of(w[j][1]) == tag) {
+                hv[2 * (half * JH + j)] = __uint_as_float((uint32_t)w[j][0]);
+                hv[2 * (half * JH + j) + 1] = __uint_as_float((uint32_t)w[j][1]);
+                got |= 1u << j;
               }
             }
+            want &= ~got;
+            if (!__any_sync(0xffffffffu, want != 0)) break;
+            if (n == 0) t0 = clock64();
+            bool bad = false;
+            if ((n & 15) == 15 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) bad = true;
+            if (clock64() - t0 > p.spin_budget) { if (lane == 0) set_status(p.hdr, MDW_ERR_TIMEOUT); bad = true; }
+            if (__any_sync(0xffffffffu, bad)) { ok = false; break; }
           }
-          ++n;
-          bool bad = false;
-          if ((n & 15) == 0 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) bad = true;
-          if (clock64() - t0 > p.spin_budget) { if (lane == 0) set_status(p.hdr, MDW_ERR_TIMEOUT); bad = true; }
-          if (__any_sync(0xffffffffu, bad)) { ok = false; break; }
         }
         if (!ok) break;
         float am = 0.f;
@@ -945,9 +1016,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
         if (writer && lane == 0) p.sh[pr] = sc;
       }
     }
+    STRACE(layer, 13);
     if (!ok) atomicExch(&tb.fail, 1);
     __syncthreads();
-    if (tb.fail) { drain_ring<MAXM>(rg); break; }
+    STRACE(layer, 7);
+    if (tb.fail) { drain_ring<MAXM>(rg, layer, has_router_rows); break; }
     // P5: down units v = warp, warp + 12, ...: slot v / U, part v % U (part 3: rows 16..)
     const int U = kDnParts + (pl.nrows > 16 ? 1 : 0);
     const int n_dn_units = S * U;
@@ -1012,9 +1085,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
         if (lane == 0 && it + SL::NS < pl.n_items) issue_item<MAXM>(p, L, tb, pl, rg, smem, it + SL::NS);
       }
     }
+    STRACE(layer, 14);
     if (!ok) atomicExch(&tb.fail, 1);
     __syncthreads();
-    if (tb.fail) { drain_ring<MAXM>(rg); break; }
+    STRACE(layer, 8);
+    if (tb.fail) { drain_ring<MAXM>(rg, layer, has_router_rows); break; }
     // combine: y[t][row] = sum over the token's pairs (ascending) of gate * s_h * dot, + residual
     {
       const uint32_t tag = (uint32_t)layer + 1;
@@ -1058,7 +1133,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_stream_kernel(const __grid_co
       }
     }
     __syncthreads();
+    STRACE(layer, 9);
   }
+  STRACE_FLUSH(p.L);
 }
 
 template <int MAXM>
@@ -1082,3 +1159,9 @@ cudaError_t launch_moe_stream(const MoeParams& p, cudaStream_t s) {
 }
 
 }  // namespace mdw
+
+#ifdef MDW_TRACE
+extern "C" int mdw_stream_trace_read(void* dst, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(dst, mdw::g_strace, bytes < sizeof(mdw::g_strace) ? bytes : sizeof(mdw::g_strace));
+}
+#endif
