@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmdw.so")
 TRACE_LIB = os.path.join(PKG, "libmdw_trace.so")     # profiling build (-DMDW_TRACE), never loaded by the API
-SOURCES = ["moe.cu", "moe_stream.cu", "lm_head.cu", "abi.cu", "noalloc.cu", "sampler.cu"]
+SOURCES = ["moe.cu", "lm_head.cu", "abi.cu", "noalloc.cu", "sampler.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=default",

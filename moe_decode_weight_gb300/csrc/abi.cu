@@ -33,12 +33,6 @@ MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
   l.header = take(kHdrWords * 4);
-  w.xr = w.xz = w.xh = 0;
-  if (M <= kStreamMaxM) {                   // zeroed with the header before every launch
-    w.xr = take((size_t)M * (kH / 2) * 8);
-    w.xz = take((size_t)M * E * 8);
-    w.xh = take(P * kI * 8);
-  }
   w.zero_end = o;
   l.xq = take((size_t)M * kH);
   l.sx = take((size_t)M * 4);
@@ -126,9 +120,6 @@ void fill_moe_ws(MoeParams& p, const MoeWs& w, uint8_t* base) {
   p.h = reinterpret_cast<float*>(base + l.h);
   p.hq = base + l.hq;
   p.sh = reinterpret_cast<float*>(base + l.sh);
-  p.xr = w.xr ? reinterpret_cast<uint64_t*>(base + w.xr) : nullptr;
-  p.xz = w.xz ? reinterpret_cast<uint64_t*>(base + w.xz) : nullptr;
-  p.xh = w.xh ? reinterpret_cast<uint64_t*>(base + w.xh) : nullptr;
 }
 }  // namespace mdw
 

@@ -62,11 +62,6 @@ struct MoeParams {
   float* h;                    // [P][I]
   uint8_t* hq;                 // [P][I]
   float* sh;                   // [P]
-  // tagged exchange words of the streaming kernel (M <= 4; zeroed before every launch):
-  // value in the low 32 bits, producing layer's tag in the high 32 bits
-  uint64_t* xr;                // [M][H/2]: residual r_l, two bf16 per word
-  uint64_t* xz;                // [M][E]: router logits
-  uint64_t* xh;                // [P][I]: SwiGLU output h per pair
 };
 
 // The LM head's cross-block merge: blocks form groups of kHeadGroupSize; each group's last
@@ -98,7 +93,6 @@ struct HeadParams {
 // Workspace layout helpers (host).
 struct MoeWs {
   mdw_moe_ws_layout lay;
-  size_t xr, xz, xh;           // tagged exchange words (streaming kernel), 0 otherwise
   size_t zero_end;             // [header, zero_end) is zeroed before every launch
   size_t resid;                // bf16 [2][M][H] ping-pong residual (stack mode)
   size_t cand;                 // head candidates (stack mode)
@@ -118,12 +112,8 @@ int head_grid();
 // Workspace pointers of one MoE launch (exchange words included).
 void fill_moe_ws(MoeParams& p, const MoeWs& w, uint8_t* base);
 
-// Launchers (return cudaSuccess or the first error). launch_moe runs windows of up to
-// kStreamMaxM tokens on the streaming kernel, larger ones on the persistent barrier kernel.
-constexpr int kStreamMaxM = 4;
+// Launchers (return cudaSuccess or the first error).
 cudaError_t launch_moe(const MoeParams& p, cudaStream_t s);
-cudaError_t launch_moe_barrier(const MoeParams& p, cudaStream_t s);
-cudaError_t launch_moe_stream(const MoeParams& p, cudaStream_t s);
 cudaError_t launch_head_fp8(const HeadParams& p, cudaStream_t s);
 cudaError_t launch_head_bf16(const HeadParams& p, cudaStream_t s);
 cudaError_t launch_quantize_head(const __nv_bfloat16* w, long long V, uint8_t* q, float* scale,

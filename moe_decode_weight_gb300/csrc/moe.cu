@@ -1447,11 +1447,6 @@ extern "C" int mdw_trace_read(void* dst, size_t bytes) {
 #endif
 
 cudaError_t launch_moe(const MoeParams& p, cudaStream_t s) {
-  if (p.M <= kStreamMaxM) return launch_moe_stream(p, s);
-  return launch_moe_barrier(p, s);
-}
-
-cudaError_t launch_moe_barrier(const MoeParams& p, cudaStream_t s) {
   if (p.M <= 1) return launch_t<1>(p, s);
   if (p.M <= 2) return launch_t<2>(p, s);
   if (p.M <= 4) return launch_t<4>(p, s);

@@ -23,8 +23,7 @@ import ctypes as C
 
 import numpy as np
 
-TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 20, 256   # the device tables' shape
-STREAM_MAX_M = 4            # windows up to this size run on the streaming kernel
+TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 20, 256   # the device table's shape
 
 # (point id, name of the phase that ends there), in kernel order; point 0 starts a layer
 PHASES = [
@@ -48,34 +47,14 @@ PHASES = [
 ]
 
 
-# The streaming kernel (windows of up to 4 tokens): thread 0 stamps these points; 3, 10-14 are
-# warp 0's own progress, the others follow a block barrier.
-STREAM_PHASES = [
-    (1, "input"),                # r poll (stack) / x read, RMSNorm, x-hat
-    (2, "router"),               # the block's router rows -> tagged logits
-    (3, "logit poll"),           # warp 0 polls token 0's logits
-    (4, "top-k+tables"),
-    (5, "issue"),                # the first ring slots requested
-    (10, "first tile wait"),     # warp 0's first gate/up tile landed
-    (11, "gate/up to last wait"),
-    (12, "gate/up last unit"),
-    (6, "gate/up block"),        # every warp's units done
-    (13, "h poll (warp 0)"),
-    (7, "h poll block"),
-    (14, "down (warp 0)"),
-    (8, "down block"),
-    (9, "combine+publish"),
-]
-
-
-def summarise(tr: np.ndarray, phases=None):
+def summarise(tr: np.ndarray):
     """tr: [layers][TRACE_POINTS][blocks] nanosecond stamps. Returns one dict per layer:
     {"total_us": first start to last B3 exit, phase name: (median_us, max_us) over blocks}."""
     out = []
     for lay in tr.astype(np.float64):
         row = {"total_us": float((lay[9].max() - lay[0].min()) / 1000.0)}
         prev = 0
-        for point, name in (phases or PHASES):
+        for point, name in PHASES:
             d = (lay[point] - lay[prev]) / 1000.0
             row[name] = (float(np.median(d)), float(d.max()))
             prev = point
@@ -127,10 +106,10 @@ def format_head(summary) -> str:
     return "\n".join(lines)
 
 
-def format_rows(rows, phases=None) -> str:
+def format_rows(rows) -> str:
     lines = ["per layer: phase median / max over blocks (us), from the previous point"]
     for l, row in enumerate(rows):
-        parts = [f"{name} {row[name][0]:.2f}/{row[name][1]:.2f}" for _, name in (phases or PHASES)]
+        parts = [f"{name} {row[name][0]:.2f}/{row[name][1]:.2f}" for _, name in PHASES]
         lines.append(f"L{l}: total {row['total_us']:.2f} | " + " | ".join(parts))
     return "\n".join(lines)
 
@@ -158,7 +137,6 @@ def main() -> None:
     layers = []
     for l in range(L):
         (w13q, w13s, w2q, w2s), sh = synth.layer_experts(3, l, synth.NUM_EXPERTS, device=dev)
-        sh = tuple(sh)
         wr = synth.router_weight(3, l, synth.NUM_EXPERTS).to(dev)
         layers.append(api.MoeWeights(wr, w13q, w13s, w2q, w2s, tuple(sh), synth.TOP_K))
     arr = api._layer_array(layers)
@@ -173,17 +151,14 @@ def main() -> None:
         torch.cuda.synchronize()
         print(f"run {it}: {e0.elapsed_time(e1) * 1000.0:.1f} us, status {api.mdw_device_status(ws)}")
     lib = api.lib()
-    stream = M <= STREAM_MAX_M                       # the kernel launch_moe picks for this window
-    reader = lib.mdw_stream_trace_read if stream else lib.mdw_trace_read
-    reader.argtypes = [C.c_void_p, C.c_size_t]
+    lib.mdw_trace_read.argtypes = [C.c_void_p, C.c_size_t]
     buf = np.zeros(TRACE_LAYERS * TRACE_POINTS * TRACE_BLOCKS, dtype=np.uint64)
-    if reader(buf.ctypes.data, buf.nbytes) != 0:
-        raise SystemExit("trace read failed")
+    if lib.mdw_trace_read(buf.ctypes.data, buf.nbytes) != 0:
+        raise SystemExit("mdw_trace_read failed")
     G = torch.cuda.get_device_properties(0).multi_processor_count
     tr = buf.reshape(TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS)[:L, :, :G]
-    phases = STREAM_PHASES if stream else PHASES
-    print(f"M = {M}, {L} layers, {G} blocks, {'streaming' if stream else 'barrier'} kernel")
-    print(format_rows(summarise(tr, phases), phases))
+    print(f"M = {M}, {L} layers, {G} blocks")
+    print(format_rows(summarise(tr)))
 
 
 def head_main(args) -> None:
