@@ -33,6 +33,8 @@ MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
   l.header = take(kHdrWords * 4);
+  w.xz = take((size_t)M * E * 8);               // zeroed with the header before every launch
+  w.xr = stack ? take((size_t)M * (kH / 2) * 8) : 0;
   w.zero_end = o;
   l.xq = take((size_t)M * kH);
   l.sx = take((size_t)M * 4);
@@ -120,6 +122,8 @@ void fill_moe_ws(MoeParams& p, const MoeWs& w, uint8_t* base) {
   p.h = reinterpret_cast<float*>(base + l.h);
   p.hq = base + l.hq;
   p.sh = reinterpret_cast<float*>(base + l.sh);
+  p.xz = reinterpret_cast<uint64_t*>(base + w.xz);
+  p.xr = w.xr ? reinterpret_cast<uint64_t*>(base + w.xr) : nullptr;
 }
 }  // namespace mdw
 
@@ -238,7 +242,7 @@ mdw_status moe_decode_layer(const mdw_moe_weights* w, int32_t M, const void* x_b
     return MDW_ERR_INVALID_ARG;
   const MoeWs lay = moe_ws_layout(M, w->num_experts, w->top_k, false, 1);
   if (ws_bytes < lay.total) return MDW_ERR_WORKSPACE_TOO_SMALL;
-  if (moe_grid() * 32 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;   // rows per block bound
+  if (moe_grid() * 16 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;   // rows per block bound
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   MoeParams* p = new MoeParams();
   fill_layer(p->layers[0], w);
@@ -394,7 +398,7 @@ mdw_status moe_decode_stack_routed(const mdw_moe_weights* layers, int32_t L, con
     return MDW_ERR_INVALID_ARG;
   const MoeWs lay = moe_ws_layout(M, E, K, true, topk);
   if (ws_bytes < lay.total) return MDW_ERR_WORKSPACE_TOO_SMALL;
-  if (moe_grid() * 32 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
+  if (moe_grid() * 16 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   MoeParams* p = new MoeParams();

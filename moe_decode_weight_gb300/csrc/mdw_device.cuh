@@ -196,6 +196,28 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
+// ------------------------------------------------------------------ tagged words
+
+// A value published for other blocks travels in an 8-byte word with the producing layer's tag
+// in the high half (an aligned 64-bit access is single-copy atomic), so the consumer's poll of
+// the word is also its read of the value: no barrier, no second round trip. The words are
+// zeroed before every launch and tags start at 1. A poll requests every word it waits for
+// before it checks any (a load whose predicate depended on the previous word's check would
+// cost one L2 round trip per word).
+__device__ __forceinline__ uint64_t tagged(uint32_t payload, uint32_t tag) { return ((uint64_t)tag << 32) | payload; }
+__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ void st_word(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void ld_word2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+}
+
 // ------------------------------------------------------------------ grid barrier
 
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {

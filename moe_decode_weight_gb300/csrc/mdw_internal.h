@@ -62,6 +62,11 @@ struct MoeParams {
   float* h;                    // [P][I]
   uint8_t* hq;                 // [P][I]
   float* sh;                   // [P]
+  // tagged words (value in the low half, producing layer + 1 in the high half; zeroed before
+  // every launch): the router logits [M][E] and (stack) the residual r_l [M][H/2], two bf16
+  // per word
+  uint64_t* xz;
+  uint64_t* xr;
 };
 
 // The LM head's cross-block merge: blocks form groups of kHeadGroupSize; each group's last
@@ -93,6 +98,7 @@ struct HeadParams {
 // Workspace layout helpers (host).
 struct MoeWs {
   mdw_moe_ws_layout lay;
+  size_t xz, xr;               // tagged logit / residual words (xr: stack only)
   size_t zero_end;             // [header, zero_end) is zeroed before every launch
   size_t resid;                // bf16 [2][M][H] ping-pong residual (stack mode)
   size_t cand;                 // head candidates (stack mode)

@@ -55,6 +55,7 @@ constexpr int kMaxSegs = 48;                    // slot segments per block list 
 constexpr int kTopkCand = 128;                  // compacted top-k candidates per warp
 constexpr int kHhBytes = kI * 2 + 64;           // f16 h-hat per pair, padded (conflict-free A loads)
 constexpr int kPairChunk = 36;                  // pairs quantised into smem at a time (all of M = 4)
+constexpr int kTaggedResidM = 2;                // windows up to this size exchange r as tagged words
 // per-warp cp.async rings (16-byte asynchronous copies into padded, bank-conflict-free rows)
 constexpr int kGuU = 8;                         // gate/up: 32-blocks per stage
 constexpr int kGuStages = 3;
@@ -175,12 +176,53 @@ __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tabl
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(smem + smem_layout(M).xb);
   uint4* xb4 = reinterpret_cast<uint4*>(xb);
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) tb.bad = 0;
+  // windows of up to kTaggedResidM tokens take r_l from tagged words; larger ones (whose
+  // staging would not fit the register budget) read the residual buffer after a barrier
+  const bool poll = MAXM <= kTaggedResidM && p.stack_mode && layer > 0;
+  if (poll) {
+    // r_l from the other blocks' tagged words (tag l): every word of this thread's chunks is
+    // requested before any is checked; the missing ones are requested again together
+    constexpr int NCH = (MAXM * CPT + kThreads - 1) / kThreads;
+    const uint32_t tag = (uint32_t)layer;
+    uint32_t want = 0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k)
+      if ((int)threadIdx.x + k * kThreads < M * CPT) want |= 1u << k;
+    long long t0 = 0;
+    for (int n = 0; want != 0; ++n) {
+      uint64_t w[NCH][4];
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) {
+        const size_t c = threadIdx.x + (size_t)k * kThreads;
+        if (want & (1u << k)) {
+          ld_word2(p.xr + 4 * c, w[k][0], w[k][1]);
+          ld_word2(p.xr + 4 * c + 2, w[k][2], w[k][3]);
+        }
+      }
+      uint32_t got = 0;
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) {
+        if ((want & (1u << k)) && tag_of(w[k][0]) == tag && tag_of(w[k][1]) == tag && tag_of(w[k][2]) == tag &&
+            tag_of(w[k][3]) == tag) {
+          xb4[threadIdx.x + k * kThreads] = make_uint4((uint32_t)w[k][0], (uint32_t)w[k][1], (uint32_t)w[k][2], (uint32_t)w[k][3]);
+          got |= 1u << k;
+        }
+      }
+      want &= ~got;
+      if (want == 0) break;
+      if (n == 0) t0 = clock64();
+      if ((n & 15) == 15 && ld_volatile_u32(p.hdr + kHdrStatus) != 0) { atomicExch(&tb.bad, 2); break; }
+      if (clock64() - t0 > p.spin_budget) { set_status(p.hdr, MDW_ERR_TIMEOUT); atomicExch(&tb.bad, 2); break; }
+    }
+    __syncthreads();
+  }
   const uint4* src = reinterpret_cast<const uint4*>(!p.stack_mode ? p.x_in : resid_ptr(p, layer));
   // Every block must derive bit-identical x and xq: per-token reductions are taken in a fixed
   // order (a warp's 32 chunks share one token; the 10 warp partials are summed in order).
   // 1. load (all threads, one 16-byte chunk each); stack: sum of squares, else: amax
   for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
-    const uint4 v = ld_cg16(src + c);
+    const uint4 v = poll ? xb4[c] : ld_cg16(src + c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float r = 0.f;
 #pragma unroll
@@ -308,7 +350,7 @@ __device__ __forceinline__ void load_router_row(const LayerDesc& L, int e, uint4
 #pragma unroll
   for (int i = 0; i < 10; ++i) wv[i] = ldg_stream16(wr + 32 * i + lane);
 }
-__device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, uint4 (&wv)[10]) {
+__device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, uint4 (&wv)[10], int layer) {
   const int M = p.M, E = p.E;
   int e0, e1;
   router_range(p, e0, e1);
@@ -331,7 +373,10 @@ __device__ void router_rows(const MoeParams& p, const LayerDesc& L, const uint8_
         }
       }
       acc = warp_sum(acc);
-      if (lane == 0) p.logits[(size_t)t * E + e] = acc;
+      if (lane == 0) {
+        st_word(p.xz + (size_t)t * E + e, tagged(__float_as_uint(acc), (uint32_t)layer + 1));
+        p.logits[(size_t)t * E + e] = acc;          // inspection copy
+      }
     }
   }
 }
@@ -405,12 +450,43 @@ __device__ void routing_tables_one(Tables& tb, int K, int first, int lane) {
   }
 }
 
+// Token t's E router logits (tag layer + 1) into v[] (v[j] = logit of expert lane + 32 j), every
+// word requested before any is checked; false (MDW_ERR_TIMEOUT recorded, or another block's
+// failure seen) when the bounded wait runs out. Warp-collective.
+__device__ bool poll_logits(const MoeParams& p, int t, int layer, float (&v)[MDW_MAX_EXPERTS / 32]) {
+  constexpr int PER = MDW_MAX_EXPERTS / 32;
+  const int lane = threadIdx.x & 31, E = p.E;
+  const uint32_t tag = (uint32_t)layer + 1;
+  const uint64_t* z = p.xz + (size_t)t * E;
+  uint32_t want = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    v[j] = -INFINITY;
+    if (lane + 32 * j < E) want |= 1u << j;
+  }
+  long long t0 = 0;
+  for (int n = 0;; ++n) {
+    uint64_t w[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) w[j] = (want & (1u << j)) ? ld_word(z + lane + 32 * j) : 0;
+    uint32_t got = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if ((want & (1u << j)) && tag_of(w[j]) == tag) { v[j] = __uint_as_float((uint32_t)w[j]); got |= 1u << j; }
+    want &= ~got;
+    if (!__any_sync(0xffffffffu, want != 0)) return true;
+    if (n == 0) t0 = clock64();
+    bool bad = (n & 15) == 15 && ld_volatile_u32(p.hdr + kHdrStatus) != 0;
+    if (clock64() - t0 > p.spin_budget) { if (lane == 0) set_status(p.hdr, MDW_ERR_TIMEOUT); bad = true; }
+    if (__any_sync(0xffffffffu, bad)) return false;
+  }
+}
+
 __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb, int layer, uint8_t* scratch) {
   const int M = p.M, E = p.E, K = p.K;
   // per-warp candidate buffers live in the gate/up partial-sum region (not live during
   // routing)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) tb.bad = 0;
   if (p.topk_override) {
     // imposed routing: [M][K] for one layer, [L][M][K] for the stack
     const int32_t* ov = p.topk_override + (p.stack_mode ? (size_t)layer * M * K : 0);
@@ -422,8 +498,20 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
           if (j != lane && ov[t * K + j] == id) ok = false;
         if (!ok) { atomicExch(&tb.bad, 1); id = 0; }
         tb.ids[t * K + lane] = id;
-        tb.gts[t * K + lane] = ld_cg_f32(p.logits + (size_t)t * E + id);
       }
+      // the imposed ids' logits: each lane polls its own word
+      const uint32_t tag = (uint32_t)layer + 1;
+      const uint64_t* z = p.xz + (size_t)t * E + (lane < K ? tb.ids[t * K + lane] : 0);
+      bool have = lane >= K;
+      uint64_t w = 0;
+      const long long t0 = clock64();
+      for (int n = 0; !__all_sync(0xffffffffu, have); ++n) {
+        if (!have) { w = ld_word(z); have = tag_of(w) == tag; }
+        bool bad = (n & 15) == 15 && ld_volatile_u32(p.hdr + kHdrStatus) != 0;
+        if (clock64() - t0 > p.spin_budget) { if (lane == 0) set_status(p.hdr, MDW_ERR_TIMEOUT); bad = true; }
+        if (__any_sync(0xffffffffu, bad)) { if (lane == 0) atomicExch(&tb.bad, 2); break; }
+      }
+      if (lane < K) tb.gts[t * K + lane] = __uint_as_float((uint32_t)w);
     }
   } else {
     // Top-K per token, one warp per token (ties -> lower expert id):
@@ -436,15 +524,14 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
     int* ci_all = reinterpret_cast<int*>(cv_all + kWarps * kTopkCand);
     int* cnt_all = ci_all + kWarps * kTopkCand;
     for (int t = warp; t < M; t += kWarps) {
-      const float* z = p.logits + (size_t)t * E;
       constexpr int PER = MDW_MAX_EXPERTS / 32;
       float v[PER];
+      if (!poll_logits(p, t, layer, v)) { if (lane == 0) atomicExch(&tb.bad, 2); break; }
       float bv = -INFINITY;
       int bi = 0x7fffffff;
 #pragma unroll
       for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
-        v[j] = e < E ? ld_cg_f32(z + e) : -INFINITY;
         if (v[j] != v[j]) v[j] = -INFINITY;            // a NaN logit ranks last (ids stay valid)
         if (e < E && beats(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
       }
@@ -1082,9 +1169,25 @@ __device__ void build_down_units(Tables& tb, int q0, int n, int nfull) {
   __syncthreads();
 }
 
+// The block's output rows [r0, r1): an equal share of the H rows; for the windows that publish
+// the residual as tagged words (two bf16 each) in whole row pairs (16 or 18 rows on 152
+// blocks), so that every word it publishes is its own; else 16 or 17 rows.
+template <int MAXM>
+__device__ __forceinline__ void out_rows(int G, int& r0, int& r1) {
+  if (MAXM <= kTaggedResidM) {
+    r0 = 2 * (int)((long long)blockIdx.x * (kH / 2) / G);
+    r1 = 2 * (int)((long long)(blockIdx.x + 1) * (kH / 2) / G);
+  } else {
+    r0 = (int)((long long)blockIdx.x * kH / G);
+    r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
+  }
+}
+
 // Output rows [r0, r1) of this block: 16-row tiles + a remainder.
+template <int MAXM>
 __device__ __forceinline__ int down_full_tiles(int G) {
-  const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
+  int r0, r1;
+  out_rows<MAXM>(G, r0, r1);
   return (r1 - r0) / 16;
 }
 
@@ -1092,7 +1195,8 @@ template <int MAXM>
 __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* smem, Tables& tb,
                              int layer, bool first_list_ready) {
   const int M = p.M, G = gridDim.x;
-  const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
+  int r0, r1;
+  out_rows<MAXM>(G, r0, r1);
   const int nrows = r1 - r0, nfull = nrows / 16, nrem = nrows - 16 * nfull;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, qd = lane & 3;
@@ -1297,15 +1401,36 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
     }
   }
   __syncthreads();
+  if (p.stack_mode) {
+    // r_{l+1} = bf16(r_l + y) for the block's rows, row pairs: into the residual buffer and,
+    // for the next layer, as tagged words (two bf16 each, tag l + 1)
+    __nv_bfloat16* rout = const_cast<__nv_bfloat16*>(resid_ptr(p, layer + 1));
+    if (MAXM > kTaggedResidM) {
+      for (int i = threadIdx.x; i < M * nrows; i += blockDim.x) {
+        const int t = i / nrows, rr = i % nrows;
+        const size_t o = (size_t)t * kH + r0 + rr;
+        rout[o] = __float2bfloat16_rn(__bfloat162float(res_in[o]) + yacc[t * kMaxRowsPerBlock + rr]);
+      }
+      return;
+    }
+    const int np = nrows / 2;
+    for (int i = threadIdx.x; i < M * np; i += blockDim.x) {
+      const int t = i / np, rr = 2 * (i % np);
+      const size_t o = (size_t)t * kH + r0 + rr;
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(__bfloat162float(res_in[o]) + yacc[t * kMaxRowsPerBlock + rr],
+                                                      __bfloat162float(res_in[o + 1]) + yacc[t * kMaxRowsPerBlock + rr + 1]);
+      const uint32_t bits = *reinterpret_cast<const uint32_t*>(&b2);
+      *reinterpret_cast<uint32_t*>(rout + o) = bits;
+      if (layer + 1 < p.L) st_word(p.xr + o / 2, tagged(bits, (uint32_t)layer + 1));
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < M * nrows; i += blockDim.x) {
     const int t = i / nrows, rr = i % nrows;
     const float y = yacc[t * kMaxRowsPerBlock + rr];
     const size_t o = (size_t)t * kH + r0 + rr;
     const float rv = (i == (int)threadIdx.x) ? res0 : (res_in ? __bfloat162float(res_in[o]) : 0.f);
-    if (p.stack_mode) {
-      __nv_bfloat16* rout = const_cast<__nv_bfloat16*>(resid_ptr(p, layer + 1));
-      rout[o] = __float2bfloat16_rn(rv + y);
-    } else {
+    {
       float v = y;
       if (p.residual) v += rv;
       if (p.y_fp32) reinterpret_cast<float*>(p.y_out)[o] = v;
@@ -1329,11 +1454,13 @@ __device__ __forceinline__ void prefetch_bulk(const uint8_t* base, size_t lo, si
 // prefetched at all (measured: requesting them right after routing delayed the warps that
 // issued them by more than the cp.async pipeline gained).
 // The block's W2 rows [r0, r1) (and scales) of every slot, dealt to every warp's lane 0.
+template <int MAXM>
 __device__ void prefetch_down_rows(const LayerDesc& L, const Tables& tb) {
   const int G = gridDim.x;
   const int warp = threadIdx.x >> 5;
   if ((threadIdx.x & 31) != 0) return;
-  const int r0 = (int)((long long)blockIdx.x * kH / G), r1 = (int)((long long)(blockIdx.x + 1) * kH / G);
+  int r0, r1;
+  out_rows<MAXM>(G, r0, r1);
   for (int s = warp; s < tb.n_slots; s += kWarps) {
     const int e = tb.slot_expert[s];
     const uint8_t* q2 = e < 0 ? L.sh_w2_q : L.w2_q + (size_t)e * kH * kW2RowBytes;
@@ -1379,17 +1506,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
       if (e0 + (int)(threadIdx.x >> 5) < e1) load_router_row(L, e0 + (threadIdx.x >> 5), wv);
       prepare_input<MAXM>(p, layer, smem, tb);
       MDW_TRACE_POINT(layer, 1);
-      router_rows(p, L, smem, wv);
+      if (tb.bad) return;                                           // the residual wait ran out
+      router_rows(p, L, smem, wv, layer);
     }
-    bar.arrive();                                                   // B1 (logits)
+    // the logits travel as tagged words (route_tokens polls them): no barrier
     if (MAXM > 16) xhat_codes_in_place(p, smem, tb);                 // the router is done with x
     MDW_TRACE_POINT(layer, 2);
     MDW_TRACE_POINT(layer, 3);
-    if (!bar.wait()) return;
     MDW_TRACE_POINT(layer, 4);
     route_tokens(p, L, tb, layer, smem + smem_layout(p.M).gured);
     __syncthreads();
-    if (tb.bad) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
+    // tb.bad: 1 = an imposed id out of range or repeated, 2 = a wait ran out (status recorded)
+    if (tb.bad) { if (threadIdx.x == 0 && tb.bad == 1) set_status(p.hdr, MDW_ERR_DEVICE_BOUNDS); return; }
     {
       // gate/up tiles of 8 row pairs of every slot (the shared expert is slot 0; 96 whole
       // tiles per slot), dealt to the blocks in equal contiguous shares of whole tiles (up to
@@ -1412,14 +1540,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
     MDW_TRACE_POINT(layer, 6);
     // during the h barrier: W2 rows into L2, the first chunk's down unit list (the gate/up
     // tile list it overwrites is finished), and the next layer's static weights
-    prefetch_down_rows(L, tb);
-    build_down_units(tb, 0, min(kPairChunk, tb.n_pairs), down_full_tiles(G));
+    prefetch_down_rows<MAXM>(L, tb);
+    build_down_units(tb, 0, min(kPairChunk, tb.n_pairs), down_full_tiles<MAXM>(G));
     if (p.stack_mode && layer + 1 < p.L) prefetch_static(p, p.layers[layer + 1]);
     if (!bar.wait()) return;
     MDW_TRACE_POINT(layer, 7);
     down_combine<MAXM>(p, L, smem, tb, layer, true);
     MDW_TRACE_POINT(layer, 8);
-    if (p.stack_mode && layer + 1 < p.L) {
+    // r_{l+1}: up to kTaggedResidM tokens it travels as tagged words (the next layer's input
+    // polls them) and no barrier is needed -- a block can only overwrite this layer's h,
+    // logits or tables after every block has published its next-layer logits, i.e. after
+    // every block has finished this layer's down phase; larger windows meet at a barrier
+    if (MAXM > kTaggedResidM && p.stack_mode && layer + 1 < p.L) {
       if (!bar.sync()) return;                                      // B3 (r_{l+1})
     }
     MDW_TRACE_POINT(layer, 9);

@@ -61,7 +61,7 @@ extern "C" mdw_status moe_decode_layer_noalloc(const mdw_moe_weights* w, int32_t
       !aligned16_or_null(topk_override) || !aligned16_or_null(topk_ids_out) ||
       !aligned16_or_null(topk_w_out) || (reinterpret_cast<uintptr_t>(device_status_out) & 3u) != 0)
     return MDW_ERR_INVALID_ARG;
-  if (moe_grid() * 32 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
+  if (moe_grid() * 16 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
   uint8_t* base = nullptr;
   st = scratch_for_current_device(&base);
   if (st != MDW_OK) return st;
