@@ -252,8 +252,9 @@ size_t mdw_lm_head_workspace_bytes(const mdw_lm_head* head, int32_t M, int32_t t
  * argmax_out int32 [M] (required); topk_idx int32 [M][topk] and topk_val fp32 [M][topk]
  * (NULL = not written; topk in 1..MDW_MAX_VOCAB_TOPK), descending, ties -> lower index.
  * head->fmt must be MDW_FMT_FP8_E4M3_ROWSCALE, else MDW_ERR_FORMAT_MISMATCH.
- * Tokens are independent here: a window of more than 16 tokens runs as launches of up to 16
- * tokens each, every launch streaming the head once (1 <= M <= MDW_MAX_M). */
+ * One launch streams the head once for the whole window (1 <= M <= MDW_MAX_M); above 2
+ * tokens it selects from fp32 logits written to `logits`, or to the workspace when NULL
+ * (mdw_lm_head_workspace_bytes then includes M * V * 4 bytes for them). */
 mdw_status lm_head_fp8(const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
                        int32_t* argmax_out, int32_t topk, int32_t* topk_idx, float* topk_val,
                        void* ws, size_t ws_bytes, mdw_stream_t stream);

@@ -26,7 +26,14 @@ int head_grid() { const int n = device_sm_count(); return n > kMaxHeadGrid ? kMa
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk) {
+// Head workspace after the header: block + group candidate lists (values, then indices) and,
+// for a window wider than kHeadListM tokens, the fp32 logits [M][V] the head selects from.
+size_t head_ws_bytes(int M, int topk, long long V) {
+  const size_t n = (size_t)(head_grid() + kHeadMaxGroups) * M * topk;
+  return 2 * align_up(n * 4, 256) + (M > kHeadListM ? align_up((size_t)M * V * 4, 256) : 0);
+}
+
+MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk, long long V) {
   MoeWs w;
   mdw_moe_ws_layout& l = w.lay;
   const size_t P = (size_t)M * (K + 1), S = (size_t)M * K + 1;
@@ -49,7 +56,7 @@ MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk) {
   l.hq = take(P * kI);
   l.sh = take(P * 4);
   w.resid = stack ? take((size_t)2 * M * kH * 2) : 0;
-  w.cand = stack ? take(head_ws_bytes(M < 16 ? M : 16, topk, head_grid())) : 0;   // one 16-token head launch
+  w.cand = stack ? take(head_ws_bytes(M, topk, V)) : 0;
   l.total = o;
   w.total = o;
   return w;
@@ -135,45 +142,34 @@ struct Draw {                     // optional draw on the final top-k
   int32_t* out = nullptr;
 };
 
-// Tokens per head launch: the head kernels are instantiated for up to 16 tokens; a larger
-// window runs as consecutive launches on the same stream (tokens are independent in the head,
-// and each launch streams the head once).
-constexpr int kHeadChunkM = 16;
-int head_chunk_m(int M) { return M < kHeadChunkM ? M : kHeadChunkM; }
-
+// One head launch for the whole window (it streams the head once): `cand` is the region
+// head_ws_bytes(M, topk, V) describes; a window wider than kHeadListM tokens selects from its
+// fp32 logits, written to `logits` when given, else to the workspace.
 mdw_status head_call(const mdw_lm_head* head, int fmt, int32_t M, const void* h_bf16, int norm_input,
                      float* logits, int32_t* argmax_out, int32_t topk, int32_t* topk_idx,
                      float* topk_val, uint32_t* hdr, uint8_t* cand, cudaStream_t s, const Draw& draw = Draw()) {
-  const size_t n = (size_t)(head_grid() + kHeadMaxGroups) * head_chunk_m(M) * topk;
-  for (int t0 = 0; t0 < M; t0 += kHeadChunkM) {
-    // later launches: the previous launch's merge counters back to zero (the status word stays)
-    if (t0 > 0 && (cudaMemsetAsync(hdr + kHdrDoneCtr, 0, 4, s) != cudaSuccess ||
-                   cudaMemsetAsync(hdr + kHdrHeadGroups, 0, kHeadMaxGroups * 4, s) != cudaSuccess))
-      return MDW_ERR_CUDA;
-    HeadParams hp{};
-    hp.sample_u = draw.u ? draw.u + t0 : nullptr;
-    hp.temperature = draw.temperature;
-    hp.top_p = draw.top_p;
-    hp.sample_out = draw.out ? draw.out + t0 : nullptr;
-    hp.w = static_cast<const uint8_t*>(head->w);
-    hp.row_scale = head->row_scale;
-    hp.V = head->vocab;
-    hp.M = M - t0 < kHeadChunkM ? M - t0 : kHeadChunkM;
-    hp.topk = topk;
-    hp.x = static_cast<const __nv_bfloat16*>(h_bf16) + (size_t)t0 * kH;
-    hp.norm_input = norm_input;
-    hp.logits = logits ? logits + (size_t)t0 * head->vocab : nullptr;
-    hp.argmax_out = argmax_out ? argmax_out + t0 : nullptr;
-    hp.topk_idx = topk_idx ? topk_idx + (size_t)t0 * topk : nullptr;
-    hp.topk_val = topk_val ? topk_val + (size_t)t0 * topk : nullptr;
-    hp.hdr = hdr;
-    hp.cand_val = reinterpret_cast<float*>(cand);
-    hp.cand_idx = reinterpret_cast<int32_t*>(cand + align_up(n * 4, 256));
-    const mdw_status st =
-        cuda_status(fmt == MDW_FMT_FP8_E4M3_ROWSCALE ? launch_head_fp8(hp, s) : launch_head_bf16(hp, s));
-    if (st != MDW_OK) return st;
-  }
-  return MDW_OK;
+  const size_t n = (size_t)(head_grid() + kHeadMaxGroups) * M * topk;
+  HeadParams hp{};
+  hp.sample_u = draw.u;
+  hp.temperature = draw.temperature;
+  hp.top_p = draw.top_p;
+  hp.sample_out = draw.out;
+  hp.w = static_cast<const uint8_t*>(head->w);
+  hp.row_scale = head->row_scale;
+  hp.V = head->vocab;
+  hp.M = M;
+  hp.topk = topk;
+  hp.x = static_cast<const __nv_bfloat16*>(h_bf16);
+  hp.norm_input = norm_input;
+  hp.logits = logits;
+  if (M > kHeadListM && !logits) hp.logits = reinterpret_cast<float*>(cand + 2 * align_up(n * 4, 256));
+  hp.argmax_out = argmax_out;
+  hp.topk_idx = topk_idx;
+  hp.topk_val = topk_val;
+  hp.hdr = hdr;
+  hp.cand_val = reinterpret_cast<float*>(cand);
+  hp.cand_idx = reinterpret_cast<int32_t*>(cand + align_up(n * 4, 256));
+  return cuda_status(fmt == MDW_FMT_FP8_E4M3_ROWSCALE ? launch_head_fp8(hp, s) : launch_head_bf16(hp, s));
 }
 
 mdw_status head_entry(int fmt, const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
@@ -301,10 +297,8 @@ mdw_status mdw_lm_head_bf16_init(const void* w_bf16, int64_t V, int32_t H, mdw_l
 
 size_t mdw_lm_head_workspace_bytes(const mdw_lm_head* head, int32_t M, int32_t topk) {
   if (!head || M < 1 || M > MDW_MAX_M || topk < 1 || topk > MDW_MAX_VOCAB_TOPK) return 0;
-  const int g = head_grid();
-  if (g <= 0) return 0;
-  const size_t n = (size_t)(g + kHeadMaxGroups) * head_chunk_m(M) * topk;   // block + group lists
-  return kHdrWords * 4 + align_up(n * 4, 256) + align_up(n * 4, 256);
+  if (head_grid() <= 0) return 0;
+  return kHdrWords * 4 + head_ws_bytes(M, topk, head->vocab);
 }
 
 mdw_status lm_head_fp8(const mdw_lm_head* head, int32_t M, const void* h_bf16, float* logits,
@@ -355,7 +349,7 @@ size_t mdw_stack_workspace_bytes(const mdw_moe_weights* layers, int32_t L, const
     E = E > layers[l].num_experts ? E : layers[l].num_experts;
     K = K > layers[l].top_k ? K : layers[l].top_k;
   }
-  return moe_ws_layout(M, E, K, true, topk).total;
+  return moe_ws_layout(M, E, K, true, topk, head ? head->vocab : 0).total;
 }
 
 mdw_status moe_decode_stack(const mdw_moe_weights* layers, int32_t L, const mdw_lm_head* head, int32_t M,
@@ -396,7 +390,7 @@ mdw_status moe_decode_stack_routed(const mdw_moe_weights* layers, int32_t L, con
   if (!al16(r0_bf16) || !al16_or_null(resid_out) || !al16(ws) ||
       (reinterpret_cast<uintptr_t>(topk_override) & 3u) != 0)
     return MDW_ERR_INVALID_ARG;
-  const MoeWs lay = moe_ws_layout(M, E, K, true, topk);
+  const MoeWs lay = moe_ws_layout(M, E, K, true, topk, head ? head->vocab : 0);
   if (ws_bytes < lay.total) return MDW_ERR_WORKSPACE_TOO_SMALL;
   if (moe_grid() * 16 < kH / 2) return MDW_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

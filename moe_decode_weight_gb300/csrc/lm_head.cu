@@ -15,7 +15,9 @@
 // per token in registers (lane i holds the i-th best), the block merges its warps' lists,
 // the last block of each group of 16 to finish merges the group's lists, and the last group
 // merges the group lists (and, when asked, draws the token from the final list). A window of
-// more than 16 tokens is several launches (the host side splits it).
+// more than kHeadListM tokens keeps no lists while streaming (per-token register lists cost
+// more than they save there): it writes its logits, and each block then selects from its own
+// rows (one warp per token), so the head is still streamed once.
 #include "mdw_device.cuh"
 #include "mdw_internal.h"
 #include "mdw_sampler.cuh"
@@ -179,35 +181,42 @@ __device__ void tree_merge(float* sv, int* si, int M, int warp, int lane) {
 
 // Loads the lists j < n of every token (list j of token t at cv / ci + ((first + j) * M + t)
 // * tk, tk entries, written by other blocks of this launch), merges them into S[t][0].
-// Warp w takes lists w, w + warps, ... of each token (n <= 2 * warps).
+// Warp w takes lists w, w + warps, ... of each token (n <= 2 * warps); the loads of up to 8
+// tokens are issued before the first merge.
 template <int MAXM>
 __device__ void merge_global_lists(const float* cv, const int* ci, int first, int n, int M, int tk,
                                    float* sv, int* si, int warp, int lane) {
-  float av[MAXM], bv[MAXM];
-  int ai[MAXM], bi[MAXM];
+  constexpr int CH = MAXM < 8 ? MAXM : 8;
+#pragma unroll 1
+  for (int t0 = 0; t0 < M; t0 += CH) {
+    float av[CH], bv[CH];
+    int ai[CH], bi[CH];
 #pragma unroll
-  for (int t = 0; t < MAXM; ++t) {             // issue every load before the first merge
-    av[t] = bv[t] = -INFINITY;
-    ai[t] = bi[t] = kPadIdx;
-    if (t < M && lane < tk) {
-      if (warp < n) {
-        const size_t o = ((size_t)(first + warp) * M + t) * tk + lane;
-        av[t] = ld_cg_f32(cv + o);
-        ai[t] = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(ci) + o));
-      }
-      if (warp + kWarps < n) {
-        const size_t o = ((size_t)(first + warp + kWarps) * M + t) * tk + lane;
-        bv[t] = ld_cg_f32(cv + o);
-        bi[t] = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(ci) + o));
+    for (int c = 0; c < CH; ++c) {
+      const int t = t0 + c;
+      av[c] = bv[c] = -INFINITY;
+      ai[c] = bi[c] = kPadIdx;
+      if (t < M && lane < tk) {
+        if (warp < n) {
+          const size_t o = ((size_t)(first + warp) * M + t) * tk + lane;
+          av[c] = ld_cg_f32(cv + o);
+          ai[c] = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(ci) + o));
+        }
+        if (warp + kWarps < n) {
+          const size_t o = ((size_t)(first + warp + kWarps) * M + t) * tk + lane;
+          bv[c] = ld_cg_f32(cv + o);
+          bi[c] = __float_as_int(ld_cg_f32(reinterpret_cast<const float*>(ci) + o));
+        }
       }
     }
-  }
 #pragma unroll
-  for (int t = 0; t < MAXM; ++t) {
-    if (t < M) {
-      if (warp + kWarps < n) list_merge(av[t], ai[t], bv[t], bi[t], lane);
-      sv[(t * kWarps + warp) * kMaxTK + lane] = av[t];
-      si[(t * kWarps + warp) * kMaxTK + lane] = ai[t];
+    for (int c = 0; c < CH; ++c) {
+      const int t = t0 + c;
+      if (t < M) {
+        if (warp + kWarps < n) list_merge(av[c], ai[c], bv[c], bi[c], lane);
+        sv[(t * kWarps + warp) * kMaxTK + lane] = av[c];
+        si[(t * kWarps + warp) * kMaxTK + lane] = ai[c];
+      }
     }
   }
   tree_merge(sv, si, M, warp, lane);
@@ -245,6 +254,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr int XS = head_x_stride<FP8>();
   constexpr int NT = (MAXM + 7) / 8;                 // 8-token column groups
+  // up to kHeadListM tokens every warp keeps its running top-k per token in registers while
+  // it walks its tiles; a wider window writes its logits (p.logits is then always given) and
+  // selects from the block's rows afterwards, one warp per token
+  constexpr bool LISTS = MAXM <= kHeadListM;
   const int M = p.M, tk = p.topk;
   uint8_t* xsm = smem;                                // [M][XS] hidden states (MMA operand)
   float* lv = reinterpret_cast<float*>(smem);         // [MAXM][warps][32] list values
@@ -262,9 +275,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   const long long v0 = blockIdx.x * p.V / G, v1 = (blockIdx.x + 1) * p.V / G;
   constexpr int ROWB = FP8 ? kH : 2 * kH;
   constexpr int NCH = ROWB / 64;                      // 64-byte chunks per row
-  constexpr int U = MDW_HEAD_U;                       // chunks per unit (loads in flight together)
+  // chunks per unit (loads in flight together); the 32-token kernel holds half as many, its
+  // accumulators taking the registers
+  constexpr int U = MAXM > 16 ? MDW_HEAD_U / 2 : MDW_HEAD_U;
   constexpr int NG = NCH / U;                         // units per tile
-  static_assert(U % 4 == 0 && NCH % U == 0, "units must tile a row in whole 128-byte lines");
+  static_assert(U % 2 == 0 && NCH % U == 0, "units must tile a row in whole 128-byte lines");
   const int ntile = (int)((v1 - v0 + 15) / 16);
   const int total = ntile * NG;
   auto ubeg = [&](int w) { return (int)((long long)w * total / kWarps); };
@@ -383,9 +398,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
   }
   MDW_HEAD_TRACE(threadIdx.x == 0, 1);
 
-  WarpList lst[MAXM];
+  WarpList lst[LISTS ? MAXM : 1];
 #pragma unroll
-  for (int t = 0; t < MAXM; ++t) list_init(lst[t]);
+  for (int t = 0; t < (LISTS ? MAXM : 1); ++t) list_init(lst[t]);
   constexpr int STEPS = FP8 ? 4 : 2;                  // k16 steps per 64-byte chunk
 
   // logits of a finished tile (sums d of rows vt + g (+8), tokens 8nt + 2q (+1)) -> lists
@@ -405,6 +420,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
         if (p.logits && okr && tok < M) p.logits[(size_t)tok * p.V + vt + g + ((j >> 1) << 3)] = lg[j];
         if (lg[j] != lg[j]) lg[j] = -INFINITY;         // a NaN logit ranks last in the top-k
       }
+      if (!LISTS) continue;
 #pragma unroll
       for (int t8 = 0; t8 < 8; ++t8) {
         const int t = 8 * nt + t8;
@@ -414,13 +430,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
           const bool mine = (q == (t8 >> 1)) && (hr ? vb_ok : va_ok);
           const float val = lg[2 * hr + (t8 & 1)];
           const int idx = (int)(vt + g + 8 * hr);
-          unsigned m = __ballot_sync(0xffffffffu, mine && beats(val, idx, lst[t].thr_v, lst[t].thr_i));
+          WarpList& Lt = lst[LISTS ? t : 0];
+          unsigned m = __ballot_sync(0xffffffffu, mine && beats(val, idx, Lt.thr_v, Lt.thr_i));
           while (m) {
             const int src = __ffs(m) - 1;
             m &= m - 1;
             const float bv = __shfl_sync(0xffffffffu, val, src);
             const int bi = __shfl_sync(0xffffffffu, idx, src);
-            list_insert(lst[t], bv, bi, tk, lane);
+            list_insert(Lt, bv, bi, tk, lane);
           }
         }
       }
@@ -552,30 +569,78 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(HeadParams p) {
     finish_tile(tL, d);
   }
 
-  // block list of every token: the warps' lists, tree-merged
+  if (LISTS) {
+    // block list of every token: the warps' lists, tree-merged
 #pragma unroll
-  for (int t = 0; t < MAXM; ++t)
-    if (t < M) {
-      lv[(t * kWarps + warp) * kMaxTK + lane] = lst[t].v;
-      li[(t * kWarps + warp) * kMaxTK + lane] = lst[t].i;
-    }
+    for (int t = 0; t < (LISTS ? MAXM : 1); ++t)
+      if (t < M) {
+        lv[(t * kWarps + warp) * kMaxTK + lane] = lst[t].v;
+        li[(t * kWarps + warp) * kMaxTK + lane] = lst[t].i;
+      }
 #ifdef MDW_TRACE
-  __syncthreads();
-  MDW_HEAD_TRACE(threadIdx.x == 0, 21);
-  if (threadIdx.x == 0) {
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    g_head_trace[blockIdx.x * 24 + 20] = smid;
-  }
+    __syncthreads();
+    MDW_HEAD_TRACE(threadIdx.x == 0, 21);
 #endif
-  tree_merge(lv, li, M, warp, lane);
-  MDW_HEAD_TRACE(threadIdx.x == 0, 22);
-  for (int t = warp; t < M; t += kWarps)
-    if (lane < tk) {
-      const size_t o = ((size_t)blockIdx.x * M + t) * tk + lane;
-      p.cand_val[o] = lv[t * kWarps * kMaxTK + lane];
-      p.cand_idx[o] = li[t * kWarps * kMaxTK + lane];
+    tree_merge(lv, li, M, warp, lane);
+    MDW_HEAD_TRACE(threadIdx.x == 0, 22);
+    for (int t = warp; t < M; t += kWarps)
+      if (lane < tk) {
+        const size_t o = ((size_t)blockIdx.x * M + t) * tk + lane;
+        p.cand_val[o] = lv[t * kWarps * kMaxTK + lane];
+        p.cand_idx[o] = li[t * kWarps * kMaxTK + lane];
+      }
+  } else {
+    // the block's logits are written (and visible to the block after the barrier); warp w
+    // walks the block's rows of tokens w, w + warps, ..., 32 rows per step and R steps of
+    // loads in flight for all its tokens at once, and its list is the block list
+    __syncthreads();
+    MDW_HEAD_TRACE(threadIdx.x == 0, 21);
+    constexpr int TPW = (MAXM + kWarps - 1) / kWarps;  // tokens per warp
+    constexpr int R = 8;
+    WarpList sel[TPW];
+#pragma unroll
+    for (int k = 0; k < TPW; ++k) list_init(sel[k]);
+    for (long long vb = v0; vb < v1; vb += 32 * R) {
+      float val[TPW][R];
+#pragma unroll
+      for (int k = 0; k < TPW; ++k) {
+        const int t = warp + k * kWarps;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const long long v = vb + 32 * r + lane;
+          val[k][r] = (t < M && v < v1) ? ld_cg_f32(p.logits + (size_t)t * p.V + v) : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < TPW; ++k) {
+        if (warp + k * kWarps >= M) break;               // warp-uniform
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const long long v = vb + 32 * r + lane;
+          const float x = val[k][r] != val[k][r] ? -INFINITY : val[k][r];
+          const int idx = (int)v;
+          unsigned m = __ballot_sync(0xffffffffu, v < v1 && beats(x, idx, sel[k].thr_v, sel[k].thr_i));
+          while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const float bv = __shfl_sync(0xffffffffu, x, src);
+            const int bi = __shfl_sync(0xffffffffu, idx, src);
+            list_insert(sel[k], bv, bi, tk, lane);
+          }
+        }
+      }
     }
+    MDW_HEAD_TRACE(threadIdx.x == 0, 22);
+#pragma unroll
+    for (int k = 0; k < TPW; ++k) {
+      const int t = warp + k * kWarps;
+      if (t < M && lane < tk) {
+        const size_t o = ((size_t)blockIdx.x * M + t) * tk + lane;
+        p.cand_val[o] = sel[k].v;
+        p.cand_idx[o] = sel[k].i;
+      }
+    }
+  }
   MDW_HEAD_TRACE(threadIdx.x == 0, 3);
 
   // the last block of each group of kHeadGroupSize blocks merges the group's lists; the last
@@ -644,15 +709,13 @@ cudaError_t launch_head_any(const HeadParams& p, cudaStream_t s) {
   if (p.M <= 1) return launch_head_t<FP8, 1>(p, s);
   if (p.M <= 2) return launch_head_t<FP8, 2>(p, s);
   if (p.M <= 4) return launch_head_t<FP8, 4>(p, s);
+  if (p.M > kHeadListM && !p.logits) return cudaErrorInvalidValue;   // it selects from its logits
   if (p.M <= 8) return launch_head_t<FP8, 8>(p, s);
-  return launch_head_t<FP8, 16>(p, s);
+  if (p.M <= 16) return launch_head_t<FP8, 16>(p, s);
+  return launch_head_t<FP8, 32>(p, s);
 }
 
 }  // namespace
-
-size_t head_ws_bytes(int M, int topk, int grid) {
-  return (size_t)(grid + kHeadMaxGroups) * M * topk * 8 + 512;
-}
 
 cudaError_t launch_head_fp8(const HeadParams& p, cudaStream_t s) { return launch_head_any<true>(p, s); }
 cudaError_t launch_head_bf16(const HeadParams& p, cudaStream_t s) { return launch_head_any<false>(p, s); }

@@ -74,6 +74,14 @@ struct MoeParams {
 constexpr int kHeadGroupSize = 16;
 constexpr int kHeadMaxGroups = 16;
 constexpr int kMaxHeadGrid = kHeadGroupSize * kHeadMaxGroups;   // blocks of the head kernel (<= 256)
+// Windows up to this many tokens keep per-warp top-k lists while the head streams; wider
+// windows write their logits and select from them (still one pass over the head). Measured
+// on the full 157,184-row FP8 head: lists 93 / 110 / 140 / 200 / 358 us at 1 / 2 / 4 / 8 /
+// 16 tokens against 117 / 121 / 124 / 130 / 170 us for logits + selection.
+#ifndef MDW_HEAD_LIST_M
+#define MDW_HEAD_LIST_M 2
+#endif
+constexpr int kHeadListM = MDW_HEAD_LIST_M;
 
 struct HeadParams {
   const uint8_t* w;            // [V][H] E4M3 or bf16 (as bytes)
@@ -104,8 +112,8 @@ struct MoeWs {
   size_t cand;                 // head candidates (stack mode)
   size_t total;
 };
-MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk);
-size_t head_ws_bytes(int M, int topk, int grid);
+MoeWs moe_ws_layout(int M, int E, int K, bool stack, int topk, long long V = 0);
+size_t head_ws_bytes(int M, int topk, long long V);
 
 // Spin budget of the kernels' bounded inter-block waits (the default, or the value set by
 // mdw_debug_set_spin_budget).

@@ -743,11 +743,15 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
   // unit descriptors held in registers: the one being requested and the one being computed
   GuUnit Ui, Uc;
   int ji = -1, jc = -1;
+  // stage counters instead of divisions by spu: the issue side is at stage `is` of unit ji,
+  // the compute side at stage `cs` of unit jc
+  int is = 0, cs = 0;
   auto issue = [&](int st) {
-    if (st / spu != ji) { ji = st / spu; Ui = info(ji); }
+    if (is == 0) { ++ji; Ui = info(ji); }
     const GuUnit& U = Ui;
     uint8_t* dst = ring + (st % STAGES) * SBYTES;
-    const int bb = U.kb0 + (st % spu) * kGuU;
+    const int bb = U.kb0 + is * kGuU;
+    if (++is == spu) is = 0;
     // token-column layout: rows of kGuPitch bytes (padded for the 4-byte fragment reads);
     // block-column layout: rows of 128 bytes, chunk b of row r at b ^ 4 (r & 1), so the
     // 16-byte reads of lanes (g, q) (rows g, chunks sb + q) hit distinct banks
@@ -778,11 +782,13 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
     cp_async_commit();
     cp_async_wait<STAGES - 1>();
     __syncwarp();
-    if (st / spu != jc) { jc = st / spu; Uc = (jc == ji) ? Ui : info(jc); }
+    if (cs == 0) { ++jc; Uc = (jc == ji) ? Ui : info(jc); }
     const GuUnit& U = Uc;
     const bool rv = g < U.nr;
     const uint8_t* buf = ring + (st % STAGES) * SBYTES;
-    const int bb = U.kb0 + (st % spu) * kGuU;
+    const int bb = U.kb0 + cs * kGuU;
+    const bool unit_end = ++cs == spu;
+    if (unit_end) cs = 0;
     if (BC) {
       constexpr int pitch = kGuU * 16;
       const uint8_t* scp = buf + 16 * pitch;
@@ -806,10 +812,10 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
         for (int j = 0; j < NT; ++j) bc_scale_add(d[j], s0 & 0xFF, s0 >> 8, s1 & 0xFF, s1 >> 8, bcacc[j]);
       }
       __syncwarp();
-      if (st % spu == spu - 1) {
+      if (unit_end) {
         float r[4];
         bc_finish<NT>(bcacc, q, r);
-        done(st / spu, r);
+        done(jc, r);
 #pragma unroll
         for (int j = 0; j < NT; ++j) bcacc[j][0] = bcacc[j][1] = 0.f;
       }
@@ -864,9 +870,9 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
       }
     }
     __syncwarp();
-    if (st % spu == spu - 1) {
+    if (unit_end) {
       const float r[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]};
-      done(st / spu, r);
+      done(jc, r);
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
     }
@@ -966,9 +972,10 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
   // busiest warp's stages, ceil(tiles * ks / warps) * 10 / ks, plus about three stages of
   // latency and epilogue per round of kGuRound units (ties: the smaller ks)
   int ks = 1, best = 1 << 30;
-  for (int c = 1; c <= 10; ++c) {
-    if (10 % c != 0) continue;
-    const int per_round = kGuRound / c * c;
+  constexpr int kParts[4] = {1, 2, 5, 10};     // the divisors of the 10 stages (constant divisions)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = kParts[i], per_round = kGuRound / c * c;
     const int rounds = (tb.gu_n * c + per_round - 1) / per_round;
     const int cost = (tb.gu_n * c + kWarps - 1) / kWarps * (10 / c) + 3 * rounds;
     if (cost < best) { best = cost; ks = c; }

@@ -28,9 +28,8 @@ TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 20, 256   # the device table's sh
 # (point id, name of the phase that ends there), in kernel order; point 0 starts a layer
 PHASES = [
     (1, "input"),                # r -> bf16 x (stack: RMSNorm) -> E4M3 x-hat
-    (2, "router+arrive"),        # router rows, arrival at the logits barrier (M > 16: x-hat codes)
-    (4, "B1 wait"),
-    (10, "top-k"),
+    (2, "router rows"),          # router rows published as tagged words (M > 16: x-hat codes)
+    (10, "logit poll+top-k"),
     (11, "tables"),
     (5, "gate/up list"),
     (15, "gate/up earlier rounds"),
@@ -43,7 +42,7 @@ PHASES = [
     (19, "down units"),
     (14, "leftover rows+sum"),
     (8, "output"),
-    (9, "B3"),
+    (9, "B3"),                   # no residual barrier up to two tokens (~0 there)
 ]
 
 

@@ -75,7 +75,7 @@ def _run_head(fn, head, h, V, k, with_logits=True):
             lg.cpu().numpy() if lg is not None else None)
 
 
-@pytest.mark.parametrize("m", [1, 4, 16, 32])
+@pytest.mark.parametrize("m", [1, 4, 16, 21, 32])
 @pytest.mark.parametrize("V,k", [(20011, 29), (1000, 29), (5003, 1), (5003, 32)])
 def test_lm_head_fp8_parity(m, V, k):
     w = _weight(V, specials=False)
@@ -90,17 +90,21 @@ def test_lm_head_fp8_parity(m, V, k):
     assert_bar(tv, np.take_along_axis(lo, ref, axis=1), "top-k values")
 
 
-def test_lm_head_fp8_without_logits_output():
+@pytest.mark.parametrize("m", [2, 32])
+def test_lm_head_fp8_without_logits_output(m):
+    """Without a logits output: above 16 tokens the head selects from logits it writes to
+    the workspace."""
     V, k = 20011, 29
     w = _weight(V, specials=False)
     head, q, s, _ = _quantize(w)
     qo, so = OL.quantize_lm_head(bf16_to_np(w))
-    h, lo = _hidden(qo, so, 2, k, seed=5)
+    h, lo = _hidden(qo, so, m, k, seed=5)
     am, ti, _, _ = _run_head(api.lm_head_fp8, head, h, V, k, with_logits=False)
     assert np.array_equal(ti, OL.topk(lo, k))
+    assert np.array_equal(am, ti[:, 0])
 
 
-@pytest.mark.parametrize("m", [1, 4])
+@pytest.mark.parametrize("m", [1, 4, 32])
 def test_lm_head_bf16_parity(m):
     V, k = 12007, 29
     w = _weight(V, specials=False)
@@ -136,7 +140,7 @@ def test_lm_head_full_vocab_codes_bit_exact(full_head):
     assert np.array_equal(q.cpu().numpy(), qo)
 
 
-@pytest.mark.parametrize("m", [1, 4])
+@pytest.mark.parametrize("m", [1, 4, 32])
 def test_lm_head_full_vocab_exact(full_head, m):
     """At the real head size: hidden states are gap-sampled by the oracle over all 157,184
     logits (its top-30 entries pairwise more than 1e-3 apart), then the fused argmax and
@@ -144,7 +148,7 @@ def test_lm_head_full_vocab_exact(full_head, m):
     head, _, _, qo, so = full_head
     V, k = synth.VOCAB, 29
     rows, los = [], []
-    for batch in range(4):
+    for batch in range(12):
         cand = torch.cat([synth.hidden_states(4000 + m, 1, 16 * batch + a) for a in range(16)], 0)
         lc = OL.lm_head_fp8_logits(qo, so, bf16_to_np(cand))
         for a in range(16):
