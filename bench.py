@@ -315,7 +315,7 @@ def _workload(m: int) -> str:
             f"bf16 pre-norm residual) + online-FP8 LM head 157184x2560 + argmax/top-29, M={m}")
 
 
-def sweep(layers, head, device, ms=(1, 2, 4, 8, 16, 32), steps: int = 3, warmup: int = 3):
+def sweep(layers, head, device, ms=(1, 2, 4, 8, 16, 32), steps: int = 5, warmup: int = 3):
     """The layer stack at several M, with the router's own routing and with Zipf(1.1)-popular
     routing imposed (seed 4 + layer): per M the step time, the mean realised union and the
     achieved GB/s of the stack (algorithmic bytes of the realised unions)."""
@@ -335,6 +335,7 @@ def sweep(layers, head, device, ms=(1, 2, 4, 8, 16, 32), steps: int = 3, warmup:
                          "layer_stack_gbs": float(np.mean(r["bytes_layers"])) / (lay * 1e6)})
             del st
         out[routing] = rows
+    out["tensor_pipe_per_m"] = tensor_pipe_per_m()
     return out
 
 
@@ -491,6 +492,19 @@ def moe_traffic(layers: int, m: int):
         return None
 
 
+def tensor_pipe_per_m():
+    """Tensor-pipe utilisation, DRAM throughput and issue activity of the MoE kernel per M from
+    the committed ncu captures (2-layer launches); None unless the kernel code still matches
+    the captured code. Counters from a profiler run, not timings of this run."""
+    try:
+        meta = json.load(open(os.path.join(ROOT, "profiles", "moe_tensor_pipe.json")))
+        if kernel_code_digest(meta["sources"]) != meta["code_sha256"]:
+            return None
+        return {"source": meta["capture"], "per_m": meta["per_m"]}
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def max_over_ranks(x: float, device, world: int) -> float:
     """The largest of every rank's x (the slowest replica sets the job's time); x itself when
     the job has one rank."""
@@ -560,6 +574,7 @@ def run_gpu(args, rank: int, world: int):
         }
         extra["heads_m1"] = time_heads(head, _w_bf16, device, m=1)
         extra["heads_m4"] = time_heads(head, _w_bf16, device, m=4)
+        extra["heads_m32"] = time_heads(head, _w_bf16, device, m=32)
         extra["sampler"] = time_sampler(head, st, device)
         extra["fp8_vs_bf16"] = fp8_vs_bf16(head, _w_bf16, device)
         extra["sweep"] = sweep(layers, head, device)
