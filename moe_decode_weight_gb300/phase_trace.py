@@ -27,9 +27,12 @@ TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 20, 256   # the device table's sh
 
 # (point id, name of the phase that ends there), in kernel order; point 0 starts a layer
 PHASES = [
+    (12, "residual poll"),       # up to two tokens in a stack: r_l from the tagged words (~0 else)
     (1, "input"),                # r -> bf16 x (stack: RMSNorm) -> E4M3 x-hat
     (2, "router rows"),          # router rows published as tagged words (M > 16: x-hat codes)
-    (10, "logit poll+top-k"),
+    (3, "logit poll"),           # (top-k warp 0; imposed routing: ~0, its wait is in "top-k rank")
+    (4, "top-k threshold"),      # lane bests, bitonic sort, the K-th best
+    (10, "top-k rank"),          # candidates compacted and ranked
     (11, "tables"),
     (5, "gate/up list"),
     (15, "gate/up earlier rounds"),
