@@ -153,7 +153,7 @@ struct Tables {
   int n_slots, n_routed, n_pairs, shared_slot, bad;
   int gu_n;                                    // entries in gu_tile
   int n_segs;                                  // slot segments of the block's gate/up share
-  int seg_slot[kMaxSegs], seg_lo[kMaxSegs], seg_hi[kMaxSegs], seg_groups[kMaxSegs], seg_off[kMaxSegs + 1];
+  int seg_slot[kMaxSegs], seg_lo[kMaxSegs], seg_groups[kMaxSegs], seg_off[kMaxSegs + 1];
   int4 gu_tile[kGuMaxTiles];                   // (slot, j0, rows, first token column)
 };
 static_assert(sizeof(Tables) <= kTablesBytes, "tables exceed the reserved shared memory");
@@ -886,41 +886,6 @@ __device__ __forceinline__ void gate_up_units(int n, int spu, Info info, Done do
   }
 }
 
-// Tile list of virtual row pairs [a, b) (slot s covers [s*kI, (s+1)*kI), slot_offset added):
-// tiles of up to 8 row pairs inside one slot, one entry per 8-token column group.
-__device__ void build_gate_up_tiles(Tables& tb, int a, int b) {
-  // thread 0 lays out the few slot segments the range touches; then every thread writes
-  // entries (segment-major, then tile, then column group)
-  if (threadIdx.x == 0) {
-    int n = 0, k = 0;
-    while (a < b && k < kMaxSegs) {
-      const int slot = a / kI, ja = a % kI, jb = min(kI, ja + (b - a));
-      const int m = tb.slot_begin[slot + 1] - tb.slot_begin[slot];
-      tb.seg_slot[k] = slot;
-      tb.seg_lo[k] = ja;
-      tb.seg_hi[k] = jb;
-      tb.seg_groups[k] = (m + 7) / 8;
-      tb.seg_off[k] = n;
-      n += (jb - ja + 7) / 8 * tb.seg_groups[k];
-      a += jb - ja;
-      ++k;
-    }
-    tb.n_segs = k;
-    tb.seg_off[k] = n;
-    tb.gu_n = (a < b || n > kGuMaxTiles) ? -1 : n;      // -1: the block's share does not fit
-  }
-  __syncthreads();
-  const int n = tb.gu_n;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    int k = 0;
-    while (i >= tb.seg_off[k + 1]) ++k;
-    const int r = i - tb.seg_off[k], gq = tb.seg_groups[k];
-    const int j0 = tb.seg_lo[k] + 8 * (r / gq);
-    tb.gu_tile[i] = make_int4(tb.seg_slot[k], j0, min(8, tb.seg_hi[k] - j0), 8 * (r % gq));
-  }
-  __syncthreads();
-}
-
 // Tile list of the kernels for more than 8 tokens, where a slot can have several 8-token
 // column groups: the work space is every (slot, tile of 8 row pairs, column group) entry,
 // slot-major, then tile, then group (slot s has 96 ceil(m_s / 8) entries), and the block takes
@@ -969,12 +934,24 @@ __device__ void build_gate_up_entries(Tables& tb, int* scratch) {
 
 // All gate/up tiles of the block's list: units (tile, K half) in rounds of kGuRound; the two
 // halves' partials are summed in a fixed order, then SwiGLU, then h per (pair, row).
+// Up to 8 tokens the list is implicit: the block's whole tiles are the virtual tiles
+// [vt0, vt0 + ntiles) (slot vt / 96, rows 8 (vt mod 96)), none cut by a slot boundary since
+// the shares are whole tiles; above, the tiles come from tb.gu_tile (tb.gu_n entries).
 template <int MAXM>
 __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint8_t* smem, Tables& tb,
-                              int trace_layer = kTraceNone) {
+                              int vt0, int ntiles, int trace_layer = kTraceNone) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   float4* red = reinterpret_cast<float4*>(const_cast<uint8_t*>(smem) + smem_layout(p.M).gured);
+  constexpr int kTilesPerSlot = kI / 8;
+  auto tile_at = [&](int i) {
+    if (MAXM <= 8) {
+      const int vt = vt0 + i;
+      return make_int4(vt / kTilesPerSlot, 8 * (vt % kTilesPerSlot), 8, 0);
+    }
+    return tb.gu_tile[i];
+  };
+  const int nt = MAXM <= 8 ? ntiles : tb.gu_n;
   // K split per tile: ks parts of 10 / ks stages (8 blocks each), chosen to minimise the
   // busiest warp's stages, ceil(tiles * ks / warps) * 10 / ks, plus about three stages of
   // latency and epilogue per round of kGuRound units (ties: the smaller ks)
@@ -983,11 +960,11 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int c = kParts[i], per_round = kGuRound / c * c;
-    const int rounds = (tb.gu_n * c + per_round - 1) / per_round;
-    const int cost = (tb.gu_n * c + kWarps - 1) / kWarps * (10 / c) + 3 * rounds;
+    const int rounds = (nt * c + per_round - 1) / per_round;
+    const int cost = (nt * c + kWarps - 1) / kWarps * (10 / c) + 3 * rounds;
     if (cost < best) { best = cost; ks = c; }
   }
-  const int units = tb.gu_n * ks;
+  const int units = nt * ks;
   const int kpart = kHBlocks / ks;
   // MMA form, fixed per kernel instantiation (each carries only its own loop, which keeps the
   // register allocation of the small-M kernels free of the other forms): block columns with
@@ -1002,7 +979,7 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
     const int mine = un > warp ? (un - warp + kWarps - 1) / kWarps : 0;
     auto info = [&](int j) {
       const int u = u0 + warp + j * kWarps;
-      const int4 t = tb.gu_tile[u / ks];
+      const int4 t = tile_at(u / ks);
       const int kp = u % ks, slot = t.x, e = tb.slot_expert[slot];
       const int pb = tb.slot_begin[slot], m = tb.slot_begin[slot + 1] - pb;
       GuUnit U;
@@ -1031,7 +1008,7 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
     MDW_TRACE_POINT(trace_layer, 16);
     for (int u = warp; u < un; u += kWarps) {
       if ((u0 + u) % ks != 0) continue;
-      const int4 t = tb.gu_tile[(u0 + u) / ks];
+      const int4 t = tile_at((u0 + u) / ks);
       float4 r = red[u * 32 + lane];
       for (int k = 1; k < ks; ++k) {
         const float4 o = red[(u + k) * 32 + lane];
@@ -1538,14 +1515,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_persistent_kernel(const __gri
       const long long T = (long long)tb.n_slots * (kI / 8);
       const int a = 8 * (int)((long long)blockIdx.x * T / G), b = 8 * (int)((long long)(blockIdx.x + 1) * T / G);
       MDW_TRACE_POINT(layer, 5);
-      if (MAXM <= 8) {
-        // up to 8 tokens every slot has one column group: equal shares of whole tiles
-        build_gate_up_tiles(tb, a, b);
-      } else {
+      if (MAXM > 8) {
+        // (up to 8 tokens every slot has one column group and the block's share is the whole
+        // tiles [a / 8, b / 8), walked without a list)
         build_gate_up_entries(tb, reinterpret_cast<int*>(smem + smem_layout(p.M).gured));
+        if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
       }
-      if (tb.gu_n < 0) { if (threadIdx.x == 0) set_status(p.hdr, MDW_ERR_UNSUPPORTED_SHAPE); return; }
-      gate_up_tiles<MAXM>(p, L, smem, tb, layer);
+      gate_up_tiles<MAXM>(p, L, smem, tb, a / 8, (b - a) / 8, layer);
     }
     bar.arrive();                                                   // B2 (h)
     MDW_TRACE_POINT(layer, 6);
