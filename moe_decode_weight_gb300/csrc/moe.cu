@@ -85,7 +85,7 @@ constexpr int kTraceNone = -1;
 // Built only with -DMDW_TRACE (a profiling build of the library, never the product build):
 // thread 0 of every block records %globaltimer at each phase boundary of every layer.
 #ifdef MDW_TRACE
-constexpr int kTracePhases = 20;
+constexpr int kTracePhases = 24;
 constexpr int kTraceLayers = 64;
 __device__ unsigned long long g_trace[kTraceLayers * kTracePhases * 256];
 #define MDW_TRACE_POINT(layer, phase)                                                        \
@@ -606,7 +606,10 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
     }
     __syncthreads();
     MDW_TRACE_POINT(layer, 10);
+    MDW_TRACE_POINT(layer, 20);
+    MDW_TRACE_POINT(layer, 21);
     MDW_TRACE_POINT(layer, 11);
+    MDW_TRACE_POINT(layer, 22);
     if (tb.bad) return;
     if (blockIdx.x == 0) publish_routing(p, tb, layer);
     return;
@@ -645,6 +648,7 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
       }
       if (act) tb.cand_g[i] = gate;
     }
+    MDW_TRACE_POINT(layer, 20);
     if (lane < MDW_MAX_EXPERTS / 32) tb.bitmap[lane] = 0;
     __syncwarp();
     for (int i = lane; i < M * K; i += 32) {
@@ -661,6 +665,7 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
       if (lane >= o) incl += nb;
     }
     if (lane < MDW_MAX_EXPERTS / 32) tb.wpre[lane] = incl - cnt;
+    MDW_TRACE_POINT(layer, 21);
     int pos = first + incl - cnt;
     for (uint32_t w = word; w; w &= w - 1) {
       tb.cnt[pos] = 0;                                  // token masks of the routed slots
@@ -708,6 +713,7 @@ __device__ void route_tokens(const MoeParams& p, const LayerDesc& L, Tables& tb,
     if (p.has_shared)
       for (int t = lane; t < M; t += 32) { tb.pair_token[t] = t; tb.pair_slot[t] = 0; tb.pair_gate[t] = 1.0f; }
   }
+  MDW_TRACE_POINT(layer, 22);
   __syncthreads();
   if (blockIdx.x == 0) publish_routing(p, tb, layer);
 }

@@ -8,7 +8,8 @@ each phase. A phase runs from the previous point in kernel order to its own poin
 
 Points inside loops (gate/up rounds, pair chunks) keep their last value, so those phases
 cover the last round / chunk, and "earlier rounds" / "earlier chunks" hold the rest.
-A one-token window builds its routing tables inside the top-k, so "tables" is ~0 there.
+A one-token window builds its routing tables inside the top-k, so "gates" .. "pairs" are ~0
+there.
 
     python -m moe_decode_weight_gb300.phase_trace --layers 8 --m 1
     python -m moe_decode_weight_gb300.phase_trace --head --m 1
@@ -23,7 +24,7 @@ import ctypes as C
 
 import numpy as np
 
-TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 20, 256   # the device table's shape
+TRACE_LAYERS, TRACE_POINTS, TRACE_BLOCKS = 64, 24, 256   # the device table's shape
 
 # (point id, name of the phase that ends there), in kernel order; point 0 starts a layer
 PHASES = [
@@ -33,7 +34,10 @@ PHASES = [
     (3, "logit poll"),           # (top-k warp 0; imposed routing: ~0, its wait is in "top-k rank")
     (4, "top-k threshold"),      # lane bests, bitonic sort, the K-th best
     (10, "top-k rank"),          # candidates compacted and ranked
-    (11, "tables"),
+    (20, "gates"),               # more than one token: softmax of the selected logits
+    (21, "union scan"),          # expert bitmap and its prefix counts
+    (11, "slots"),               # the union's slots (one token: all tables, in registers)
+    (22, "pairs"),               # token masks, slot offsets, the pair lists
     (5, "gate/up list"),
     (15, "gate/up earlier rounds"),
     (16, "gate/up last round"),
