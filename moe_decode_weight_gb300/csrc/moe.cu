@@ -19,17 +19,20 @@
 //   per layer, every block
 //   P0  the weights of its router row are requested first; (stack) x = bf16(RMSNorm(r_l))
 //       and (all) xq = E4M3(x / sx), computed redundantly by every block from the 5 KB/token
-//       input, so no exchange is needed;
-//   P1  router logits for its slice of the E router rows -> global; B1;
-//   P2  top-k + dedup redundantly from the E x M logits (every block derives the same slot /
-//       pair tables; slot 0 is the shared expert);
+//       input (up to two tokens r_l arrives as tagged words the previous layer's blocks
+//       published, above two it is read after the residual barrier B3);
+//   P1  router logits for its slice of the E router rows, published as tagged words (value
+//       and layer tag in one 8-byte word), so no barrier is needed before the top-k;
+//   P2  top-k + dedup redundantly from the E x M logits, which the top-k warps poll (every
+//       block derives the same slot / pair tables; slot 0 is the shared expert);
 //   P3  gate/up for its contiguous share of the (slot, row-pair tile) space -- of the
 //       (slot, tile, 8-token column group) space above 8 tokens -> h; arrive(B2); while
 //       waiting: bulk L2 prefetch of its W2 rows of every slot and (stack) of the next
 //       layer's router rows and shared-expert slice; wait(B2);
 //   P4  every block quantises all pairs' h (amax / 448) into shared memory, then computes
 //       its slice of output rows over all slots (no atomics: a fixed summation order);
-//       (stack) r_{l+1} = bf16(r_l + y); B3.
+//       (stack) r_{l+1} = bf16(r_l + y), up to two tokens also published as tagged words,
+//       above two followed by B3.
 //   The expert GEMVs run on m16n8k16 tensor-core MMAs: with up to four tokens the MMA
 //   columns carry (token, K-block) pairs (block-column form, one or two tiles, scales applied
 //   per column in fp32); with more tokens they carry tokens, the E8M0 scale folded into the
