@@ -240,16 +240,30 @@ __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tabl
     xb4[c] = v;
   }
   __syncthreads();
+  // up to 4 tokens (at most 4 chunks per thread) every thread derives a token's 1/rms and
+  // scale itself from the warps' partials, in the same order as the one thread would, instead
+  // of one thread per token and a block barrier after it; the amax partials then go to a
+  // second array so no partial is overwritten while another warp may still read it
+  constexpr bool kSelf = MAXM <= 4;
+  float* part_am = tb.part + (kSelf && p.stack_mode ? MAXM * (CPT / 32) : 0);
+  auto token_inv = [&](int t) {
+    float ss = 0.f;
+    for (int g = 0; g < CPT / 32; ++g) ss += tb.part[t * (CPT / 32) + g];
+    return rsqrtf(ss / (float)kH + 1e-6f);
+  };
+  auto token_scale = [&](int t) {
+    float am = 0.f;
+    for (int g = 0; g < CPT / 32; ++g) am = fmaxf(am, part_am[t * (CPT / 32) + g]);
+    return am > 0.f ? __fdiv_rn(am, kE4M3Max) : 1.0f;
+  };
   if (p.stack_mode) {
     // 2. x = bf16(r * rsqrt(mean(r^2) + eps)), then its amax
-    if (threadIdx.x < M) {
-      float ss = 0.f;
-      for (int g = 0; g < CPT / 32; ++g) ss += tb.part[threadIdx.x * (CPT / 32) + g];
-      tb.inv_rms[threadIdx.x] = rsqrtf(ss / (float)kH + 1e-6f);
+    if (!kSelf) {
+      if (threadIdx.x < M) tb.inv_rms[threadIdx.x] = token_inv(threadIdx.x);
+      __syncthreads();
     }
-    __syncthreads();
     for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
-      const float inv = tb.inv_rms[c / CPT];
+      const float inv = kSelf ? token_inv(c / CPT) : tb.inv_rms[c / CPT];
       const uint4 v = xb4[c];
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
       float am = 0.f;
@@ -261,26 +275,35 @@ __device__ void prepare_input(const MoeParams& p, int layer, uint8_t* smem, Tabl
         am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
       }
       am = warp_max(am);
-      if (lane == 0) tb.part[c / 32] = am;
+      if (lane == 0) part_am[c / 32] = am;
       xb4[c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
     __syncthreads();
   }
   // 3. per-token scale = amax/448 (IEEE division), then codes: x/scale correctly rounded,
   //    round-to-nearest-even saturating conversion; x-hat (f16) into the planes layout
-  if (threadIdx.x < M) {
-    float am = 0.f;
-    for (int g = 0; g < CPT / 32; ++g) am = fmaxf(am, tb.part[threadIdx.x * (CPT / 32) + g]);
-    const float sc = am > 0.f ? __fdiv_rn(am, kE4M3Max) : 1.0f;
-    tb.sx[threadIdx.x] = sc;
-    if (blockIdx.x == 0) p.sx[threadIdx.x] = sc;
+  if (!kSelf) {
+    if (threadIdx.x < M) {
+      const float sc = token_scale(threadIdx.x);
+      tb.sx[threadIdx.x] = sc;
+      if (blockIdx.x == 0) p.sx[threadIdx.x] = sc;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (MAXM > 16) return;                          // codes written after the router (xhat_codes_in_place)
   const bool writer = (blockIdx.x == 0);
   for (int c = threadIdx.x; c < M * CPT; c += blockDim.x) {
     const int t = c / CPT, i = c % CPT;           // chunk i = elements 8i .. 8i+7 of token t
-    const float sc = tb.sx[t];
+    float sc;
+    if (kSelf) {
+      sc = token_scale(t);
+      if (i == 0) {                               // one writer per token (read after the last barrier)
+        tb.sx[t] = sc;
+        if (blockIdx.x == 0) p.sx[t] = sc;
+      }
+    } else {
+      sc = tb.sx[t];
+    }
     const uint4 v = xb4[c];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t q[4], h[4];
@@ -1037,7 +1060,9 @@ __device__ void gate_up_tiles(const MoeParams& p, const LayerDesc& L, const uint
         }
       }
     }
-    __syncthreads();
+    // the partial sums are reused by the next round; after the last one the caller's barrier
+    // arrival (a block barrier first) follows
+    if (u0 + round < units) __syncthreads();
   }
 }
 
@@ -1238,7 +1263,9 @@ __device__ void down_combine(const MoeParams& p, const LayerDesc& L, uint8_t* sm
   };
   for (int q0 = 0; q0 < NP; q0 += kPairChunk) {
     const int n = min(kPairChunk, NP - q0);
-    __syncthreads();
+    // a later chunk overwrites the h-hat, partials and list of the previous one (the first
+    // follows the h barrier's block barrier, after which nothing here is still being read)
+    if (q0 > 0) __syncthreads();
     MDW_TRACE_POINT(layer, 17);
     quantise_pairs(p, smem, tb, q0, n);
     MDW_TRACE_POINT(layer, 18);
