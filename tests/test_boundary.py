@@ -164,3 +164,21 @@ def test_workspace_regions_hold_their_arrays(m):
     names = [n for n, _ in api.MoeWsLayoutC._fields_]
     for a, b in zip(names, names[1:]):
         assert getattr(lay, b) - getattr(lay, a) >= need[a], a
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 32])
+def test_stack_workspace_holds_the_head_logits_above_two_tokens(m):
+    """Above two tokens the head selects from fp32 logits it writes to the workspace, so the
+    stack's workspace grows by at least M * V * 4 bytes when a head is given; up to two tokens
+    the head keeps its lists in registers and needs only the candidate lists."""
+    lib = api.lib()
+    V = 157184
+    head = api.LMHeadC(api.MDW_MAGIC, api.FMT_FP8, V, 2560, 0, FAKE, FAKE)
+    layers = (api.MoeWeightsC * 1)(_weights())
+    with_head = lib.mdw_stack_workspace_bytes(layers, 1, C.byref(head), m, 29)
+    without = lib.mdw_stack_workspace_bytes(layers, 1, None, m, 29)
+    assert with_head > without > 0
+    if m > 2:
+        assert with_head - without >= m * V * 4
+    else:
+        assert with_head - without < m * V * 4
