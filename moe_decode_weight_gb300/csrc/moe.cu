@@ -53,7 +53,7 @@ constexpr int kXhBytes = kH * 2 + 64;           // f16 x-hat per token, padded (
 constexpr int kXh8Bytes = kH + 32;              // E4M3 x-hat per token (M > 16), padded likewise
 constexpr int kTablesBytes = 18432;             // shared memory reserved for the per-block tables
 constexpr int kGuRound = 4 * kWarps;            // gate/up units per round (partials in smem)
-constexpr int kGuMaxTiles = 320;                // (tile, token-tile) entries per block
+constexpr int kGuMaxTiles = 320;                // list entries per block (gate/up above 8 tokens, down units)
 constexpr int kMaxSegs = 48;                    // slot segments per block list (>= kPairChunk + 1)
 constexpr int kTopkCand = 128;                  // compacted top-k candidates per warp
 constexpr int kHhBytes = kI * 2 + 64;           // f16 h-hat per pair, padded (conflict-free A loads)
@@ -155,9 +155,10 @@ struct Tables {
   float sh[kPairChunk];
   int n_slots, n_routed, n_pairs, shared_slot, bad;
   int gu_n;                                    // entries in gu_tile
-  int n_segs;                                  // slot segments of the block's gate/up share
+  int n_segs;                                  // slot segments of the current down pair chunk
   int seg_slot[kMaxSegs], seg_lo[kMaxSegs], seg_groups[kMaxSegs], seg_off[kMaxSegs + 1];
-  int4 gu_tile[kGuMaxTiles];                   // (slot, j0, rows, first token column)
+  int4 gu_tile[kGuMaxTiles];                   // gate/up above 8 tokens: (slot, j0, rows, first token
+                                               // column); down: (slot, tile, K half, first pair)
 };
 static_assert(sizeof(Tables) <= kTablesBytes, "tables exceed the reserved shared memory");
 
